@@ -1,0 +1,456 @@
+#!/usr/bin/env python3
+"""Benchmark of the mHC forward hot path on GB300 (one JSON line on rank 0).
+
+A step is one ``mhc_forward`` (GEMM+RMS, coefficients + Sinkhorn, pre-apply,
+post/res-apply) over one batch of the prefill workload B=16384, n=4, C=7168
+(X 940 MB bf16), inputs resident in HBM.  X is far larger than L2 (129 MB),
+so no L2 flush is needed between steps.
+
+Reported:
+  value        tokens/s over all ranks (weak scaling: every rank runs its own batch)
+  e2e          the same metric through the public API with pinned host buffers:
+               H2D of the step's inputs, the forward, D2H of its outputs, all timed
+  roofline     the dominant kernel's algorithmic bytes / its CUDA-event time,
+               against the measured HBM copy bandwidth (MEASURED_PEAKS.json)
+  cpu_baseline the fp64 oracle on the host cores, on a bounded token sample
+  clocks       nvidia-smi samples taken while the timed steps run
+
+``--impl reference`` times the fp64 oracle instead (host cores only).
+Under torchrun (N > 1) each rank drives its own GPU; rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "mHC fwd tokens/s & achieved HBM GB/s vs ~8 TB/s (B=16384,n=4,C=7168)"
+WORKLOAD = "prefill"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS = ("gemm_rms", "coeffs", "pre_apply", "post_res_apply")
+# kernel -> source file whose contents the stored DRAM counters were taken from
+KERNEL_SOURCES = {"gemm_rms": "gemm_rms.cu", "coeffs": "coeffs.cu",
+                  "pre_apply": "apply.cu", "post_res_apply": "apply.cu"}
+
+
+def algorithmic_bytes(B: int, n: int, C: int) -> dict:
+    """Compulsory HBM bytes per launch of each kernel (read once, write once)."""
+    K, N = n * C, n * n + 2 * n
+    X, Fc = 2 * B * K, 2 * B * C
+    H = 4 * B * (2 * n + n * n)
+    return {
+        "gemm_rms": X + 2 * N * K + 4 * B * N + 4 * B,
+        "coeffs": 4 * B * N + 4 * B + 4 * N + H,
+        "pre_apply": X + 4 * B * n + Fc,
+        "post_res_apply": X + Fc + 4 * B * n * n + 4 * B * n + X,
+    }
+
+
+def measured_peaks() -> tuple:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "MEASURED_PEAKS.json hbm_gbs (of measured)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "profiling-recipe fallback 6.8 TB/s (of fallback)"
+
+
+def stored_traffic(kernel: str):
+    """DRAM bytes per launch from a committed ncu capture, or None if stale/absent."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        ent = d[kernel]
+        src = os.path.join(ROOT, "gemm_rms_sinkhorn_gb300", "csrc", KERNEL_SOURCES[kernel])
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if ent.get("source_sha256_16") != digest:
+            return None
+        return int(ent["bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (SM clock, throttle reasons) with host arrival times."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        mx = [num(p[1]) for p in win if num(p[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "power_w_max": max((num(p[2]) or 0.0) for p in win), "samples": len(win)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+def cpu_oracle_rate(wl, inp, budget_s: float, chunk: int = 128):
+    """Tokens/s of the fp64 oracle forward on the first tokens of the workload,
+    in chunks of `chunk` tokens until `budget_s` seconds of oracle time."""
+    import oracle
+
+    phi = np.ascontiguousarray(inp["phi_t"].T)
+    done, elapsed = 0, 0.0
+    B = inp["X"].shape[0]
+    while elapsed < budget_s and done < B:
+        rows = min(chunk, B - done)
+        X, F = inp["X"][done:done + rows], inp["F_out"][done:done + rows]
+        t = time.perf_counter()
+        oracle.forward(X, phi, F, wl.n, wl.C, wl.alpha_pre, wl.alpha_post, wl.alpha_res,
+                       inp["bias"], wl.iters)
+        elapsed += time.perf_counter() - t
+        done += rows
+    return done / elapsed, done, elapsed
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    # each step: the oracle forward over a bounded sample of the workload's tokens
+    tokens_per_step = args.ref_tokens
+    import oracle
+    import synth
+
+    inp = synth.make_inputs(wl, 0, rows=tokens_per_step)
+    phi = np.ascontiguousarray(inp["phi_t"].T)
+
+    def step():
+        oracle.forward(inp["X"], phi, inp["F_out"], wl.n, wl.C, wl.alpha_pre, wl.alpha_post,
+                       wl.alpha_res, inp["bias"], wl.iters)
+
+    for _ in range(args.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t
+    value = tokens_per_step * args.steps / el
+    sample = "first %d tokens of %s per step (fp64 oracle, 1 thread)" % (tokens_per_step,
+                                                                         wl.name)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": workload_config(wl, 1),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, world):
+    return {"workload": "mHC forward prefill B=%d n=%d C=%d iters=%d" % (wl.B, wl.n, wl.C,
+                                                                         wl.iters),
+            "B_per_gpu": wl.B, "n": wl.n, "C": wl.C, "K": wl.K, "N": wl.N, "iters": wl.iters,
+            "global_batch_tokens": wl.B * world, "parallelism": "replicas%d" % world,
+            "l2": "no flush: inputs larger than L2 (X %.0f MB > 129 MB)" % (2 * wl.B * wl.K / 1e6)}
+
+
+# ------------------------------------------------------- rank combination
+
+
+def max_over_ranks(x: float, dist=None, device=None) -> float:
+    """The slowest rank's time: every rank gets the maximum of `x`."""
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def tokens_per_second(tokens_per_rank: int, world: int, steps: int, ms_total: float) -> float:
+    """Whole-job throughput: the tokens every rank processed over the slowest rank's time."""
+    return tokens_per_rank * world * steps / (ms_total / 1e3)
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--ref-tokens", type=int, default=128,
+                    help="tokens per step of the --impl reference arm")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+
+    import synth
+
+    wl = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist = dist_mod
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    import gemm_rms_sinkhorn_gb300 as mhc
+
+    B, n, C = wl.B, wl.n, wl.C
+    inp = synth.make_inputs(wl, seed=rank)
+
+    def to_dev_bf16(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    X = to_dev_bf16(inp["X"])
+    F_out = to_dev_bf16(inp["F_out"])
+    phi_t = to_dev_bf16(inp["phi_t"])
+    bias = torch.from_numpy(inp["bias"]).to(dev)
+    out = mhc.alloc_outputs(B, n, C, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        mhc.mhc_forward(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                        wl.iters, B, n, C, out["Y"], out["r"], out["H_pre"], out["H_post"],
+                        out["H_res"], out["F_pre"], out["X_next"], out["ws"], stream)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+
+    # ---- timed region: K whole forward steps
+    for _ in range(args.warmup):
+        step()
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    # keep the same load up for ~1 s when the timed region is short, so the
+    # clock samples describe the loaded state of the timed steps
+    t_host1 = time.time()
+    extra_until = t_host0 + 1.0
+    while time.time() < extra_until:
+        for _ in range(20):
+            step()
+        torch.cuda.synchronize(dev)
+    t_host2 = time.time()
+    ms_total = max_over_ranks(ms_total, dist, dev)
+    ms_step = ms_total / args.steps
+    value = tokens_per_second(B, world, args.steps, ms_total)
+
+    # ---- per-kernel CUDA-event times over the same steps (same stream)
+    nk = len(KERNELS)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+           for _ in range(args.steps)]
+    barrier()
+    for s in range(args.steps):
+        e = evs[s]
+        e[0].record(stream)
+        mhc.mhc_gemm_rms(X, phi_t, B, n, C, out["Y"], out["r"], out["ws"], stream)
+        e[1].record(stream)
+        mhc.mhc_coeffs(out["Y"], out["r"], wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                       wl.iters, B, n, out["H_pre"], out["H_post"], out["H_res"], stream)
+        e[2].record(stream)
+        mhc.mhc_pre_apply(X, out["H_pre"], B, n, C, out["F_pre"], stream)
+        e[3].record(stream)
+        mhc.mhc_post_res_apply(X, F_out, out["H_res"], out["H_post"], B, n, C, out["X_next"],
+                               stream)
+        e[4].record(stream)
+    barrier()
+    per_kernel_ms = {k: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1])
+                                         for s in range(args.steps))
+                     for i, k in enumerate(KERNELS)}
+    sampler.stop()
+    status = mhc.mhc_device_status()
+    if status != mhc.MHC_OK:
+        raise RuntimeError("device status %s after the timed steps" % mhc.mhc_status_str(status))
+
+    algo = algorithmic_bytes(B, n, C)
+    peak, peak_src = measured_peaks()
+    dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
+    achieved = algo[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
+    total_bytes = sum(algo.values())
+    kernels_json = {k: {"ms": per_kernel_ms[k], "algorithmic_bytes": algo[k],
+                        "GBps": algo[k] / (per_kernel_ms[k] / 1e3) / 1e9,
+                        "frac": algo[k] / (per_kernel_ms[k] / 1e3) / 1e9 / peak}
+                    for k in KERNELS}
+
+    # ---- end to end through the public API with pinned host buffers
+    h_X = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
+    h_X.copy_(X)
+    h_F = torch.empty(F_out.shape, dtype=F_out.dtype, pin_memory=True)
+    h_F.copy_(F_out)
+    h_phi = phi_t.cpu().pin_memory()
+    h_bias = bias.cpu().pin_memory()
+    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
+             for k, v in out.items() if k != "ws"}
+    d_in = {"X": torch.empty_like(X), "F": torch.empty_like(F_out),
+            "phi": torch.empty_like(phi_t), "bias": torch.empty_like(bias)}
+
+    def e2e_step():
+        d_in["X"].copy_(h_X, non_blocking=True)
+        d_in["F"].copy_(h_F, non_blocking=True)
+        d_in["phi"].copy_(h_phi, non_blocking=True)
+        d_in["bias"].copy_(h_bias, non_blocking=True)
+        mhc.mhc_forward(d_in["X"], d_in["phi"], d_in["F"], wl.alpha_pre, wl.alpha_post,
+                        wl.alpha_res, d_in["bias"], wl.iters, B, n, C, out["Y"], out["r"],
+                        out["H_pre"], out["H_post"], out["H_res"], out["F_pre"], out["X_next"],
+                        out["ws"], stream)
+        for k, v in h_out.items():
+            v.copy_(out[k], non_blocking=True)
+
+    h2d = sum(t.numel() * t.element_size() for t in (h_X, h_F, h_phi, h_bias))
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.e2e_steps
+    e2e_value = tokens_per_second(B, world, 1, e2e_ms)
+
+    # ---- CPU baseline: the fp64 oracle on the host cores (rank 0 only)
+    cpu = None
+    if rank == 0 and world == 1:
+        rate, tokens, secs = cpu_oracle_rate(wl, inp, args.cpu_budget)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d tokens of B=%d n=%d C=%d, fp64 oracle forward, %.1f s" % (
+                   tokens, B, n, C, secs), "cpu": cpu_model(), "host_cores": os.cpu_count()}
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+    clocks = sampler.summary(t_host0, max(t_host1, t_host2))
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; X rows N(0, s^2), s log-uniform"
+                " in [0.1, 10])",
+        "config": workload_config(wl, world),
+        "hbm_GBps_forward": total_bytes / (ms_step / 1e3) / 1e9,
+        "roofline_forward": {"algorithmic_bytes": total_bytes, "peak": peak,
+                             "frac": total_bytes / (ms_step / 1e3) / 1e9 / peak},
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": stored_traffic(dom),
+                     "algorithmic_bytes": algo[dom], "peak_source": peak_src},
+        "kernels": kernels_json,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

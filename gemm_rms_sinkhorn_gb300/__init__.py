@@ -1,0 +1,186 @@
+"""Python binding of the GB300 mHC forward library (``include/mhc.h``).
+
+Argument marshalling only: every step of the mHC forward runs in the CUDA
+kernels of ``libmhc_gb300.so``.  PyTorch supplies device memory and streams.
+Importing this package raises ``ImportError`` when the library has not been
+built (``python -m gemm_rms_sinkhorn_gb300.build``); there is no fallback.
+
+Functions carry the C names and take torch tensors in the layouts of
+``mhc.h`` (bf16 tensors as ``torch.bfloat16``, fp32 as ``torch.float32``, all
+contiguous CUDA tensors).  ``stream`` defaults to torch's current stream.
+A non-zero status raises ``MhcError``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmhc_gb300.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError("%s is missing: build it with `python -m gemm_rms_sinkhorn_gb300.build` "
+                      "(or __graft_entry__.build())" % LIB_PATH)
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+MHC_OK = 0
+MHC_ERR_INVALID = -1
+MHC_ERR_UNSUPPORTED = -2
+MHC_ERR_ALIGN = -3
+MHC_ERR_CUDA = -4
+MHC_ERR_TIMEOUT = -5
+MHC_ERR_WORKSPACE = -6
+
+_vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                              ctypes.c_size_t)
+_SIGS = {
+    "mhc_status_str": ([_i32], ctypes.c_char_p),
+    "mhc_workspace_bytes": ([_i64, _i32, _i64], _sz),
+    "mhc_gemm_rms": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_coeffs": ([_vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
+    "mhc_pre_apply": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
+    "mhc_post_res_apply": ([_vp, _vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
+    "mhc_forward": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                     _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class MhcError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, mhc_status_str(status)))
+
+
+def mhc_status_str(status: int) -> str:
+    return _lib.mhc_status_str(status).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MHC_OK:
+        raise MhcError(status, where)
+
+
+def _ptr(t, dtype, name):
+    """Device pointer of a contiguous CUDA tensor of `dtype` (None -> NULL)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    if not (isinstance(ws, torch.Tensor) and ws.is_cuda and ws.is_contiguous()):
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def mhc_workspace_bytes(B: int, n: int, C: int) -> int:
+    return int(_lib.mhc_workspace_bytes(B, n, C))
+
+
+def workspace(B: int, n: int, C: int, device=None) -> torch.Tensor:
+    """A device buffer of ``mhc_workspace_bytes(B, n, C)`` bytes (at least 16)."""
+    nbytes = max(16, mhc_workspace_bytes(B, n, C))
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def mhc_gemm_rms(X, phi_t, B, n, C, Y, r, ws, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_gemm_rms(_ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), B, n, C,
+                             _ptr(Y, f, "Y"), _ptr(r, f, "r"), p, nb, _stream(stream)),
+           "mhc_gemm_rms")
+
+
+def mhc_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre, H_post, H_res,
+               stream=None):
+    f = torch.float32
+    _check(_lib.mhc_coeffs(_ptr(Y, f, "Y"), _ptr(r, f, "r"), alpha_pre, alpha_post, alpha_res,
+                           _ptr(bias, f, "bias"), iters, B, n, _ptr(H_pre, f, "H_pre"),
+                           _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"), _stream(stream)),
+           "mhc_coeffs")
+
+
+def mhc_pre_apply(X, H_pre, B, n, C, F_pre, stream=None):
+    _check(_lib.mhc_pre_apply(_ptr(X, torch.bfloat16, "X"), _ptr(H_pre, torch.float32, "H_pre"),
+                              B, n, C, _ptr(F_pre, torch.bfloat16, "F_pre"), _stream(stream)),
+           "mhc_pre_apply")
+
+
+def mhc_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    _check(_lib.mhc_post_res_apply(_ptr(X, bf, "X"), _ptr(F_out, bf, "F_out"),
+                                   _ptr(H_res, f, "H_res"), _ptr(H_post, f, "H_post"), B, n, C,
+                                   _ptr(X_next, bf, "X_next"), _stream(stream)),
+           "mhc_post_res_apply")
+
+
+def mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_forward(_ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), _ptr(F_out, bf, "F_out"),
+                            alpha_pre, alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n,
+                            C, _ptr(Y, f, "Y"), _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"),
+                            _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"),
+                            _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
+                            _stream(stream)),
+           "mhc_forward")
+
+
+def mhc_device_status() -> int:
+    st = _i32(0)
+    _check(_lib.mhc_device_status(ctypes.byref(st)), "mhc_device_status")
+    return st.value
+
+
+def alloc_outputs(B: int, n: int, C: int, device=None) -> dict:
+    """Output buffers of ``mhc_forward`` for (B, n, C) plus its workspace."""
+    dev = device or "cuda"
+    N = n * n + 2 * n
+    f, bf = torch.float32, torch.bfloat16
+    return dict(Y=torch.empty(B, N, dtype=f, device=dev), r=torch.empty(B, dtype=f, device=dev),
+                H_pre=torch.empty(B, n, dtype=f, device=dev),
+                H_post=torch.empty(B, n, dtype=f, device=dev),
+                H_res=torch.empty(B, n, n, dtype=f, device=dev),
+                F_pre=torch.empty(B, C, dtype=bf, device=dev),
+                X_next=torch.empty(B, n * C, dtype=bf, device=dev),
+                ws=workspace(B, n, C, dev))
+
+
+def forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, n, C, out=None,
+            stream=None) -> dict:
+    """``mhc_forward`` on tensors; allocates outputs when ``out`` is None."""
+    B = X.shape[0]
+    o = out if out is not None else alloc_outputs(B, n, C, X.device)
+    mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                o["Y"], o["r"], o["H_pre"], o["H_post"], o["H_res"], o["F_pre"], o["X_next"],
+                o["ws"], stream)
+    return o

@@ -1,0 +1,275 @@
+// C ABI of the mHC forward library (declared in include/mhc.h): argument
+// validation on the host, then the kernels of gemm_rms.cu, coeffs.cu and
+// apply.cu on the caller's stream.  No exception crosses this boundary and
+// nothing here allocates device memory.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mhc.h"
+#include "mhc_internal.h"
+
+namespace mhc {
+
+cudaError_t current_device_info(DeviceInfo *info)
+{
+    constexpr int kMaxDevices = 64;
+    static DeviceInfo cache[kMaxDevices];
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev].device == dev) {
+            *info = cache[dev];
+            return cudaSuccess;
+        }
+    }
+    DeviceInfo d;
+    d.device = dev;
+    if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev)) !=
+        cudaSuccess)
+        return e;
+    if ((e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev)) !=
+        cudaSuccess)
+        return e;
+    if (dev >= 0 && dev < kMaxDevices) {
+        std::lock_guard<std::mutex> lock(mu);
+        cache[dev] = d;
+    }
+    *info = d;
+    return cudaSuccess;
+}
+
+namespace {
+
+struct Buf {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlaps(const Buf &a, const Buf &b)
+{
+    if (a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape rules shared by every call.  Returns MHC_OK or the error.
+int check_shape(int64_t B, int n, int64_t C, bool needs_c)
+{
+    if (B < 0) return MHC_ERR_INVALID;
+    if (n < 1 || n > 8) return MHC_ERR_UNSUPPORTED;
+    if (needs_c) {
+        if (C < 8 || C % 8 != 0) return MHC_ERR_UNSUPPORTED;
+        // K = n*C is addressed with 32-bit TMA coordinates and int kernel arguments
+        if (static_cast<int64_t>(n) * C > (int64_t{1} << 30)) return MHC_ERR_UNSUPPORTED;
+    }
+    if (B > (int64_t{1} << 40)) return MHC_ERR_UNSUPPORTED;
+    return MHC_OK;
+}
+
+int check_ptrs(const Buf *bufs, int count)
+{
+    for (int i = 0; i < count; ++i)
+        if (bufs[i].p == nullptr) return MHC_ERR_INVALID;
+    for (int i = 0; i < count; ++i)
+        if (!aligned16(bufs[i].p)) return MHC_ERR_ALIGN;
+    return MHC_OK;
+}
+
+// Outputs must not overlap inputs or each other.  `alias_ok` names one
+// (output, input) pair that may be exactly equal.
+int check_overlap(const Buf *outs, int n_out, const Buf *ins, int n_in, const void *alias_out,
+                  const void *alias_in)
+{
+    for (int i = 0; i < n_out; ++i) {
+        for (int j = 0; j < n_in; ++j) {
+            if (outs[i].p == alias_out && ins[j].p == alias_in && alias_out == alias_in &&
+                outs[i].bytes == ins[j].bytes)
+                continue;
+            if (overlaps(outs[i], ins[j])) return MHC_ERR_INVALID;
+        }
+        for (int j = i + 1; j < n_out; ++j)
+            if (overlaps(outs[i], outs[j])) return MHC_ERR_INVALID;
+    }
+    return MHC_OK;
+}
+
+int check_device(DeviceInfo *info)
+{
+    if (current_device_info(info) != cudaSuccess) return MHC_ERR_CUDA;
+    if (info->cc_major != 10 || info->cc_minor != 3) return MHC_ERR_UNSUPPORTED;
+    return MHC_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
+
+size_t bf16_bytes(int64_t count) { return static_cast<size_t>(count) * 2; }
+size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
+
+#define MHC_TRY(expr)                   \
+    do {                                \
+        const int st_ = (expr);         \
+        if (st_ != MHC_OK) return st_;  \
+    } while (0)
+
+}  // namespace
+}  // namespace mhc
+
+using namespace mhc;
+
+extern "C" {
+
+const char *mhc_status_str(int status)
+{
+    switch (status) {
+    case MHC_OK: return "MHC_OK";
+    case MHC_ERR_INVALID: return "MHC_ERR_INVALID: bad size, NULL pointer, overlap or iters < 0";
+    case MHC_ERR_UNSUPPORTED: return "MHC_ERR_UNSUPPORTED: n, C or device not supported";
+    case MHC_ERR_ALIGN: return "MHC_ERR_ALIGN: pointer not 16-byte aligned";
+    case MHC_ERR_CUDA: return "MHC_ERR_CUDA: CUDA runtime call or launch failed";
+    case MHC_ERR_TIMEOUT: return "MHC_ERR_TIMEOUT: a bounded device wait ran out";
+    case MHC_ERR_WORKSPACE: return "MHC_ERR_WORKSPACE: workspace missing or too small";
+    default: return "unknown mhc status";
+    }
+}
+
+size_t mhc_workspace_bytes(int64_t B, int n, int64_t C)
+{
+    if (check_shape(B, n, C, true) != MHC_OK) return 0;
+    DeviceInfo info;
+    if (current_device_info(&info) != cudaSuccess) return 0;
+    return gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+}
+
+int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C, float *Y,
+                 float *r, void *workspace, size_t workspace_bytes, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 2));
+    MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[2].bytes = need;
+    MHC_TRY(check_ptrs(outs + 2, 1));
+    MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    return cuda_status(launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post, float alpha_res,
+               const float *bias, int iters, int64_t B, int n, float *H_pre, float *H_post,
+               float *H_res, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, 8, false));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const Buf ins[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {bias, f32_bytes(N)}};
+    const Buf outs[] = {{H_pre, f32_bytes(B * n)}, {H_post, f32_bytes(B * n)},
+                        {H_res, f32_bytes(B * n * n)}};
+    MHC_TRY(check_ptrs(ins, 3));
+    MHC_TRY(check_ptrs(outs, 3));
+    MHC_TRY(check_overlap(outs, 3, ins, 3, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
+                                     H_pre, H_post, H_res, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_pre_apply(const mhc_bf16 *X, const float *H_pre, int64_t B, int n, int64_t C,
+                  mhc_bf16 *F_pre, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const Buf ins[] = {{X, bf16_bytes(B * n * C)}, {H_pre, f32_bytes(B * n)}};
+    const Buf outs[] = {{F_pre, bf16_bytes(B * C)}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(
+        launch_pre_apply(X, H_pre, B, n, C, F_pre, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_res,
+                       const float *H_post, int64_t B, int n, int64_t C, mhc_bf16 *X_next,
+                       mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const Buf ins[] = {{X, bf16_bytes(B * n * C)}, {F_out, bf16_bytes(B * C)},
+                       {H_res, f32_bytes(B * n * n)}, {H_post, f32_bytes(B * n)}};
+    const Buf outs[] = {{X_next, bf16_bytes(B * n * C)}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out, float alpha_pre,
+                float alpha_post, float alpha_res, const float *bias, int iters, int64_t B, int n,
+                int64_t C, float *Y, float *r, float *H_pre, float *H_post, float *H_res,
+                mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,
+                mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)},
+                       {F_out, bf16_bytes(B * C)}, {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {F_pre, bf16_bytes(B * C)},
+                  {X_next, bf16_bytes(B * K)},   {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 7));
+    MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[7].bytes = need;
+    MHC_TRY(check_ptrs(outs + 7, 1));
+    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
+    if (e == cudaSuccess)
+        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre, H_post,
+                          H_res, s);
+    if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
+    return cuda_status(e);
+}
+
+int mhc_device_status(int *status)
+{
+    if (status == nullptr) return MHC_ERR_INVALID;
+    int v = 0;
+    if (read_and_clear_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
+    *status = v;
+    return MHC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,172 @@
+// Step 4 of the mHC forward: the two bandwidth-bound apply kernels (page
+// "mHC 算法分析 & cutile 高效实现", §2.5; fusion §3.4; §5.4 uses plain FMAs,
+// not MMA, for the n×n mixing).
+//
+//   pre:       F_pre[b][c]     = Σ_i H_pre[b][i]·X[b][i][c]
+//   post/res:  X_next[b][i][c] = Σ_j H_res[b][i][j]·X[b][j][c] + H_post[b][i]·F_out[b][c]
+//
+// A thread owns 8 consecutive channels c of one token: it reads them from all
+// n streams with 128-bit loads, mixes in fp32 and writes 128-bit stores, so X
+// is read once and every output written once, fully coalesced.  A block
+// covers a run of channels of one token (blockIdx.y walks the tokens), and
+// the token's coefficients are staged once per block in shared memory.
+// Streaming cache hints (.cs) keep the single-use data from displacing L2.
+//
+// In place: X_next may equal X.  Every thread loads all its inputs before it
+// stores, and the addresses it stores are exactly the ones it loaded, which
+// no other thread touches; the accesses are volatile asm, kept in order.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "mhc_internal.h"
+#include "ptx.cuh"
+
+namespace mhc {
+namespace {
+
+constexpr int kMaxGridY = 65535;
+
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
+{
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&f)[8])
+{
+    return make_uint4(pack_bf16_rn(f[0], f[1]), pack_bf16_rn(f[2], f[3]),
+                      pack_bf16_rn(f[4], f[5]), pack_bf16_rn(f[6], f[7]));
+}
+
+template <int n>
+__global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__restrict__ H_pre,
+                                 int64_t B, int64_t C, uint16_t *__restrict__ F_pre)
+{
+    const int64_t C8 = C >> 3;
+    const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        float h[n];
+#pragma unroll
+        for (int i = 0; i < n; ++i) h[i] = __ldg(H_pre + b * n + i);
+        if (c8 < C8) {
+            const uint16_t *x = X + b * n * C + c8 * 8;
+            uint4 xv[n];
+#pragma unroll
+            for (int i = 0; i < n; ++i) xv[i] = ptx::ld_stream_v4(x + i * C);
+            float acc[8], t[8];
+            unpack8(xv[0], t);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = h[0] * t[e];
+#pragma unroll
+            for (int i = 1; i < n; ++i) {
+                unpack8(xv[i], t);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(h[i], t[e], acc[e]);
+            }
+            ptx::st_stream_v4(F_pre + b * C + c8 * 8, pack8(acc));
+        }
+    }
+}
+
+template <int n>
+__global__ void post_res_apply_kernel(const uint16_t *X, const uint16_t *__restrict__ F_out,
+                                      const float *__restrict__ H_res,
+                                      const float *__restrict__ H_post, int64_t B, int64_t C,
+                                      uint16_t *X_next)
+{
+    __shared__ float hs[n * n + n];
+    const int64_t C8 = C >> 3;
+    const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        __syncthreads();  // previous token's coefficients are no longer read
+        for (int t = threadIdx.x; t < n * n + n; t += blockDim.x)
+            hs[t] = t < n * n ? __ldg(H_res + b * n * n + t) : __ldg(H_post + b * n + (t - n * n));
+        __syncthreads();
+        if (c8 < C8) {
+            const uint16_t *x = X + b * n * C + c8 * 8;
+            uint4 xv[n];
+#pragma unroll
+            for (int j = 0; j < n; ++j) xv[j] = ptx::ld_stream_v4(x + j * C);
+            const uint4 fv = ptx::ld_stream_v4(F_out + b * C + c8 * 8);
+            float f[8];
+            unpack8(fv, f);
+            uint16_t *y = X_next + b * n * C + c8 * 8;
+#pragma unroll
+            for (int i = 0; i < n; ++i) {
+                float acc[8], t[8];
+                const float hp = hs[n * n + i];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+                for (int j = 0; j < n; ++j) {
+                    const float hij = hs[i * n + j];
+                    unpack8(xv[j], t);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(hij, t[e], acc[e]);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) acc[e] = fmaf(hp, f[e], acc[e]);
+                ptx::st_stream_v4(y + i * C, pack8(acc));
+            }
+        }
+    }
+}
+
+// Threads per block: a power of two that divides C/8 when one exists (no idle
+// lanes), otherwise 128.
+int block_threads(int64_t C8)
+{
+    for (int t : {256, 128, 64, 32})
+        if (C8 % t == 0) return t;
+    return 128;
+}
+
+dim3 apply_grid(int64_t B, int64_t C8, int threads)
+{
+    const int64_t gx = (C8 + threads - 1) / threads;
+    const int64_t gy = B < kMaxGridY ? B : kMaxGridY;
+    return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+}
+
+}  // namespace
+
+cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, int n, int64_t C,
+                             uint16_t *F_pre, cudaStream_t stream)
+{
+    const int64_t C8 = C / 8;
+    const int threads = block_threads(C8);
+    const dim3 grid = apply_grid(B, C8, threads);
+    switch (n) {
+#define MHC_CASE(k) \
+    case k: pre_apply_kernel<k><<<grid, threads, 0, stream>>>(X, H_pre, B, C, F_pre); break;
+        MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
+        MHC_CASE(8)
+#undef MHC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_post_res_apply(const uint16_t *X, const uint16_t *F_out, const float *H_res,
+                                  const float *H_post, int64_t B, int n, int64_t C,
+                                  uint16_t *X_next, cudaStream_t stream)
+{
+    const int64_t C8 = C / 8;
+    const int threads = block_threads(C8);
+    const dim3 grid = apply_grid(B, C8, threads);
+    switch (n) {
+#define MHC_CASE(k)                                                                         \
+    case k:                                                                                 \
+        post_res_apply_kernel<k><<<grid, threads, 0, stream>>>(X, F_out, H_res, H_post, B, C, \
+                                                                 X_next);                   \
+        break;
+        MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
+        MHC_CASE(8)
+#undef MHC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace mhc

@@ -1,0 +1,507 @@
+// Step 1 of the mHC forward: the skinny projection GEMM fused with the RMS
+// reduction (page "mHC 算法分析 & cutile 高效实现", §2.1, §2.2, fusion §3.1;
+// split-K motivation §5.1).
+//
+//   Y[b][k] = Σ_q X[b][q]·φ[q][k]    r[b] = sqrt(Σ_q X[b][q]² / K)
+//
+// Design (sm_103a):
+//   * Work unit = one 128-token × 64-K block.  Units are ordered tile-major
+//     (all K blocks of token tile 0, then tile 1, ...) and split into equal
+//     contiguous ranges, one per persistent CTA (stream-K), so every SM gets
+//     the same number of units whatever B and K are.  N is tiny (24 or 80),
+//     so output tiling alone would leave most SMs idle (§5.1).
+//   * Warp 0 streams X and φᵀ tiles with TMA (128-byte swizzle) through a
+//     multi-stage mbarrier ring.  Warp 1 issues tcgen05.mma (M=128,
+//     N=NPAD, K=16, bf16 in, fp32 accumulate) into a double-buffered TMEM
+//     accumulator.  Warps 2-5 sum x² for their 32 rows straight from the same
+//     shared-memory tiles (X is read from HBM once) and run the epilogue
+//     (tcgen05.ld of the accumulator).
+//   * A tile covered by several CTAs is finished by the last one to arrive
+//     (atomic ticket): it adds the partial sums in contributor order, so
+//     the result is bitwise reproducible (§5.2 sums the splits in a fixed
+//     order too).
+//   * Every mbarrier wait is bounded; on expiry the CTA raises the device
+//     status word, drains what it started, frees TMEM and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "mhc_internal.h"
+#include "ptx.cuh"
+
+namespace mhc {
+namespace {
+
+constexpr int kBM = 128;       // tokens per tile (MMA M)
+constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row
+constexpr int kThreads = 192;  // 6 warps: TMA, MMA, 4 × square-sum/epilogue
+constexpr int kEpiThreads = 128;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of GPU time per wait
+constexpr int kStatusTimeout = -5;                // MHC_ERR_TIMEOUT
+
+__device__ int g_device_status;
+
+template <int NPAD>
+struct Cfg {
+    static constexpr int kABytes = kBM * kBK * 2;
+    static constexpr int kBBytes = NPAD * kBK * 2;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStages = (200 * 1024) / kStageBytes;
+    static constexpr int kTmemCols =
+        2 * NPAD <= 32 ? 32 : (2 * NPAD <= 64 ? 64 : (2 * NPAD <= 128 ? 128 : 256));
+    static constexpr int kBarrierBytes = 256;
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+    static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "MMA N for M=128");
+    static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(kStages >= 4, "pipeline depth");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    static_assert((2 * kStages + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
+};
+
+// Static stream-K schedule: CTA c owns units [lo(c), lo(c+1)).
+struct Sched {
+    int64_t total;  // m_tiles * kbt
+    int kbt;        // K blocks per token tile
+    int m_tiles;
+    int grid;
+    __host__ __device__ int64_t lo(int c) const { return total * c / grid; }
+    // The CTA whose range holds unit u.
+    __host__ __device__ int owner(int64_t u) const {
+        return static_cast<int>(((u + 1) * grid - 1) / total);
+    }
+};
+
+struct Segment {
+    int m, k0, k1;
+};
+
+// Walks the segments (one token tile, a contiguous K-block range) of a CTA.
+struct SegIter {
+    int64_t u, end;
+    int kbt;
+    __device__ bool next(Segment &s) {
+        if (u >= end) return false;
+        s.m = static_cast<int>(u / kbt);
+        s.k0 = static_cast<int>(u - static_cast<int64_t>(s.m) * kbt);
+        int64_t left = end - u;
+        s.k1 = left < kbt - s.k0 ? s.k0 + static_cast<int>(left) : kbt;
+        u += s.k1 - s.k0;
+        return true;
+    }
+};
+
+// Group barrier of the 128 epilogue threads on an mbarrier, so that the wait
+// is bounded like every other wait in the kernel.
+__device__ __forceinline__ bool epi_sync(uint64_t *bar, uint32_t &phase, volatile int *abort_flag) {
+    ptx::mbar_arrive(bar);
+    const bool ok = ptx::mbar_wait_bounded(bar, phase, abort_flag, kWaitLimitNs);
+    phase ^= 1;
+    return ok;
+}
+
+__device__ __forceinline__ void raise_timeout(volatile int *abort_flag) {
+    *abort_flag = 1;
+    atomicExch(&g_device_status, kStatusTimeout);
+}
+
+template <int NPAD>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
+                int *__restrict__ tile_tickets, float *__restrict__ partials)
+{
+    using C = Cfg<NPAD>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+    uint64_t *empty = full + C::kStages;
+    uint64_t *acc_full = empty + C::kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;       // [2]
+    uint64_t *epi_bar = acc_empty + 2;        // epilogue group barrier
+    uint64_t *drain_bar = epi_bar + 1;        // MMA drain after an abort
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+    volatile int *is_last = reinterpret_cast<volatile int *>(tmem_holder + 2);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], 1 + 4);  // MMA commit + one arrive per square-sum warp
+        }
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&acc_full[a], 1);
+            ptx::mbar_init(&acc_empty[a], 4);
+        }
+        ptx::mbar_init(epi_bar, kEpiThreads);
+        ptx::mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        *is_last = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_x);
+        ptx::prefetch_tensormap(&tm_w);
+    }
+    if (warp == 1) ptx::tmem_alloc<C::kTmemCols>(tmem_holder);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    const int64_t u_begin = sch.lo(cta), u_end = sch.lo(cta + 1);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_x = ptx::policy_evict_first();  // X streams through once
+            const uint64_t pol_w = ptx::policy_evict_last();   // φ is re-read by every CTA
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            SegIter it{u_begin, u_end, sch.kbt};
+            Segment sg;
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                for (int kb = sg.k0; kb < sg.k1; ++kb) {
+                    if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag,
+                                                kWaitLimitNs)) {
+                        raise_timeout(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *a = smem + stage * C::kStageBytes;
+                    ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    ptx::tma_load_2d(a, &tm_x, kb * kBK, sg.m * kBM, &full[stage], pol_x);
+                    ptx::tma_load_2d(a + C::kABytes, &tm_w, kb * kBK, 0, &full[stage], pol_w);
+                    ++issued;
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                }
+            }
+            if (!ok) {
+                // Let the copies already issued land before shared memory is released:
+                // the last min(issued, stages) stages each hold one outstanding phase.
+                int64_t pending = issued < C::kStages ? issued : C::kStages;
+                int s = stage;
+                uint32_t ph = phase;
+                for (int64_t i = 0; i < pending; ++i) {
+                    if (--s < 0) { s = C::kStages - 1; ph ^= 1; }
+                    volatile int never = 0;
+                    ptx::mbar_wait_bounded(&full[s], ph, &never, kWaitLimitNs);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, NPAD);
+            int stage = 0;
+            uint32_t phase = 0;
+            int seg = 0;
+            SegIter it{u_begin, u_end, sch.kbt};
+            Segment sg;
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                const int acc = seg & 1;
+                if (!ptx::mbar_wait_bounded(&acc_empty[acc], ((seg >> 1) & 1) ^ 1, abort_flag,
+                                            kWaitLimitNs)) {
+                    raise_timeout(abort_flag);
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPAD);
+                for (int kb = sg.k0; kb < sg.k1; ++kb) {
+                    if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                        raise_timeout(abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = ptx::smem_u32(smem + stage * C::kStageBytes);
+                    const uint64_t a_desc = ptx::smem_desc_sw128(a_addr);
+                    const uint64_t b_desc = ptx::smem_desc_sw128(a_addr + C::kABytes);
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk) {
+                        // advancing K by 16 bf16 = 32 bytes inside the swizzle row
+                        ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
+                                      (kb > sg.k0 || kk > 0) ? 1u : 0u);
+                    }
+                    ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
+                    if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+                }
+                if (!ok) break;
+                ptx::mma_commit(&acc_full[acc]);
+                ++seg;
+            }
+            // Before TMEM is released every MMA issued must have completed: a
+            // commit arrives only after all prior tcgen05 ops of this thread.
+            if (!ok || *abort_flag) {
+                ptx::mma_commit(drain_bar);
+                volatile int never = 0;
+                ptx::mbar_wait_bounded(drain_bar, 0, &never, kWaitLimitNs);
+            }
+        }
+    } else {
+        // ------------------------------- square-sum + epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 64;  // 0..127 within the epilogue group
+        int stage = 0;
+        uint32_t phase = 0, epi_phase = 0;
+        int seg = 0;
+        SegIter it{u_begin, u_end, sch.kbt};
+        Segment sg;
+        bool ok = true;
+        while (ok && it.next(sg)) {
+            float ss0 = 0.f, ss1 = 0.f, ss2 = 0.f, ss3 = 0.f;
+            for (int kb = sg.k0; kb < sg.k1; ++kb) {
+                if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                    raise_timeout(abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint8_t *arow = smem + stage * C::kStageBytes + row * 128;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // 16-byte chunk j of the row lives at chunk (j ^ row%8) (128-byte
+                    // swizzle); a row sum needs every chunk once, in any order.
+                    const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+                    float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y), a3 = bf16_hi(v.y);
+                    float a4 = bf16_lo(v.z), a5 = bf16_hi(v.z), a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
+                    ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
+                    ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
+                    ss0 = fmaf(a4, a4, ss0); ss1 = fmaf(a5, a5, ss1);
+                    ss2 = fmaf(a6, a6, ss2); ss3 = fmaf(a7, a7, ss3);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&empty[stage]);
+                if (++stage == C::kStages) { stage = 0; phase ^= 1; }
+            }
+            if (!ok) break;
+
+            // accumulator of this segment -> registers
+            const int acc = seg & 1;
+            if (!ptx::mbar_wait_bounded(&acc_full[acc], (seg >> 1) & 1, abort_flag, kWaitLimitNs)) {
+                raise_timeout(abort_flag);
+                break;
+            }
+            ptx::tc_fence_after();
+            float v[NPAD];
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * NPAD);
+#pragma unroll
+            for (int j = 0; j < NPAD / 16; ++j) {
+                float t[16];
+                ptx::tmem_ld_16(taddr + j * 16, t);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[j * 16 + e] = t[e];
+            }
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+            ++seg;
+
+            const float ss = (ss0 + ss1) + (ss2 + ss3);
+            const int64_t row0 = static_cast<int64_t>(sg.m) * kBM;
+            const int64_t grow = row0 + row;
+            if (sg.k0 == 0 && sg.k1 == sch.kbt) {
+                // the whole K range of this tile is ours: write the result
+                if (grow < B) {
+                    float *y = Y + grow * N;
+#pragma unroll
+                    for (int j = 0; j < NPAD; ++j)
+                        if (j < N) y[j] = v[j];
+                    r[grow] = sqrtf(ss / static_cast<float>(K));
+                }
+                continue;
+            }
+            // partial: park [row][N+1] in this (cta, tile) slot, then take a ticket
+            const int stride = N + 1;
+            float *mine = partials + static_cast<int64_t>(cta + sg.m) * kBM * stride;
+            if (grow < B) {
+#pragma unroll
+                for (int j = 0; j < NPAD; ++j)
+                    if (j < N) mine[row * stride + j] = v[j];
+                mine[row * stride + N] = ss;
+            }
+            __threadfence();
+            if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
+            const int first = sch.owner(static_cast<int64_t>(sg.m) * sch.kbt);
+            const int last = sch.owner(static_cast<int64_t>(sg.m + 1) * sch.kbt - 1);
+            if (et == 0) {
+                const int prev = atomicAdd(&tile_tickets[sg.m], 1);
+                *is_last = (prev == last - first);
+            }
+            if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
+            if (*is_last) {
+                __threadfence();
+                // fixed-order sum over the contributors first..last
+                const int64_t rows = (B - row0) < kBM ? (B - row0) : kBM;
+                const int items = static_cast<int>(rows) * stride;
+                const int64_t slot0 = static_cast<int64_t>(first + sg.m);
+                for (int i = et; i < items; i += kEpiThreads) {
+                    float s = 0.f;
+                    for (int c = 0; c <= last - first; ++c)
+                        s += __ldcg(partials + (slot0 + c) * kBM * stride + i);
+                    const int rr = i / stride, cc = i - rr * stride;
+                    if (cc < N)
+                        Y[(row0 + rr) * N + cc] = s;
+                    else
+                        r[row0 + rr] = sqrtf(s / static_cast<float>(K));
+                }
+                if (et == 0) tile_tickets[sg.m] = 0;
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<Cfg<NPAD>::kTmemCols>(tmem_base);
+    }
+}
+
+// ------------------------------------------------------------------ host
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows)
+{
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int npad_of(int n)
+{
+    const int N = num_coeffs(n);
+    return (N + 15) / 16 * 16;
+}
+
+// Grid: one CTA per SM, but no more than 32 contributors per token tile (the
+// last arriver's fixed-order sum grows with the fan-in) and at least one K
+// block per CTA.
+Sched make_sched(int64_t B, int n, int64_t C, int num_sms)
+{
+    Sched s;
+    s.m_tiles = static_cast<int>((B + kBM - 1) / kBM);
+    s.kbt = static_cast<int>((n * C + kBK - 1) / kBK);
+    s.total = static_cast<int64_t>(s.m_tiles) * s.kbt;
+    int64_t g = num_sms;
+    if (g > 32LL * s.m_tiles) g = 32LL * s.m_tiles;
+    if (g > s.total) g = s.total;
+    if (g < 1) g = 1;
+    s.grid = static_cast<int>(g);
+    return s;
+}
+
+size_t tickets_bytes(int m_tiles) { return (static_cast<size_t>(m_tiles) * 4 + 255) / 256 * 256; }
+
+template <int NPAD>
+cudaError_t launch_npad(const CUtensorMap &tx, const CUtensorMap &tw, int64_t B, int N, int K,
+                        const Sched &s, float *Y, float *r, int *tickets, float *partials,
+                        cudaStream_t stream, int device)
+{
+    using Cf = Cfg<NPAD>;
+    static uint64_t configured = 0;  // one bit per device
+    static std::mutex mu;
+    if (device < 64 && !((configured >> device) & 1)) {
+        std::lock_guard<std::mutex> lock(mu);
+        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cf::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured |= 1ull << device;
+    }
+    gemm_rms_kernel<NPAD><<<s.grid, kThreads, Cf::kSmemBytes, stream>>>(tx, tw, B, N, K, s, Y, r,
+                                                                       tickets, partials);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
+{
+    if (B <= 0) return 0;
+    const Sched s = make_sched(B, n, C, num_sms);
+    const int N = num_coeffs(n);
+    const size_t slots = static_cast<size_t>(s.grid) + s.m_tiles;
+    return tickets_bytes(s.m_tiles) + slots * kBM * (N + 1) * sizeof(float);
+}
+
+cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
+                            int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                            cudaStream_t stream)
+{
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Sched s = make_sched(B, n, C, num_sms);
+    CUtensorMap tx, tw;
+    const int npad = npad_of(n);
+    if (!make_tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
+        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                   static_cast<uint32_t>(npad)))
+        return cudaErrorInvalidValue;
+    int *tickets = static_cast<int *>(workspace);
+    float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                                tickets_bytes(s.m_tiles));
+    cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(s.m_tiles) * 4, stream);
+    if (e != cudaSuccess) return e;
+    int device = 0;
+    if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    const int Ki = static_cast<int>(K);
+    switch (npad) {
+    case 16: return launch_npad<16>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
+    case 32: return launch_npad<32>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
+    case 48: return launch_npad<48>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
+    case 64: return launch_npad<64>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
+    case 80: return launch_npad<80>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_device_status(int *status)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    int v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_device_status, sizeof v)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero)) != cudaSuccess) return e;
+    *status = v;
+    return cudaSuccess;
+}
+
+}  // namespace mhc

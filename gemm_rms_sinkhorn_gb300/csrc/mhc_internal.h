@@ -1,0 +1,43 @@
+// Launchers shared between the translation units of the library.  Arguments
+// have already been validated by the C ABI layer (api.cu) when these run.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace mhc {
+
+// N = n² + 2n coefficient columns per token.
+inline int num_coeffs(int n) { return n * n + 2 * n; }
+
+// Cached per-device facts (SM count, compute capability).
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int cc_major = 0;
+    int cc_minor = 0;
+};
+cudaError_t current_device_info(DeviceInfo *info);
+
+// ---- step 1: GEMM + RMS (gemm_rms.cu)
+size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
+                            int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                            cudaStream_t stream);
+cudaError_t read_and_clear_device_status(int *status);
+
+// ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
+cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,
+                          const float *bias, int iters, int64_t B, int n, float *H_pre,
+                          float *H_post, float *H_res, cudaStream_t stream);
+
+// ---- step 4: apply kernels (apply.cu)
+cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, int n, int64_t C,
+                             uint16_t *F_pre, cudaStream_t stream);
+cudaError_t launch_post_res_apply(const uint16_t *X, const uint16_t *F_out, const float *H_res,
+                                  const float *H_post, int64_t B, int n, int64_t C,
+                                  uint16_t *X_next, cudaStream_t stream);
+
+}  // namespace mhc

@@ -1,0 +1,156 @@
+/*
+ * mhc.h — C ABI of the GB300 (sm_103a) mHC forward library.
+ *
+ * Manifold-constrained hyper-connections (mHC) widen the residual stream of a
+ * transformer into n parallel streams and mix them with per-token
+ * coefficients.  This library computes the forward pass of that mixing as
+ * analysed on the page "mHC 算法分析 & cutile 高效实现" (mHC algorithm
+ * analysis and an efficient cuTile implementation), §2.1–§2.5 and §3:
+ *
+ *   mhc_gemm_rms        Ỹ = X·φ and r = sqrt(Σx²/(nC))          (§2.1, §2.2, §3.1)
+ *   mhc_coeffs          H̃ = α·Ỹ/r + b; H_pre = σ(H̃_pre),
+ *                       H_post = 2σ(H̃_post), H_res = Sinkhorn(H̃_res) (§2.3, §2.4, §3.2, §3.3)
+ *   mhc_pre_apply       F_pre = Σ_i H_pre[i]·X[i]                 (§2.5)
+ *   mhc_post_res_apply  X_next[i] = Σ_j H_res[i][j]·X[j] + H_post[i]·F_out (§2.5, §3.4)
+ *   mhc_forward         the four calls above, in order, on one stream
+ *
+ * Shapes: B tokens (batch × sequence), expansion n, hidden size C,
+ * K = n·C, N = n² + 2n.
+ *
+ * Layouts (all row-major, densely packed, no strides):
+ *   X, X_next  [B][n][C] bf16   the n streams of a token side by side (= [B][K])
+ *   phi_t      [N][K]    bf16   φᵀ: the projection φ ∈ R^{K×N} transposed, K contiguous
+ *   F_out      [B][C]    bf16   output of the layer function F (F lies outside mHC)
+ *   F_pre      [B][C]    bf16
+ *   Y          [B][N]    fp32   columns [0,n) pre, [n,2n) post, [2n,N) res (row-major n×n)
+ *   r          [B]       fp32
+ *   bias       [N]       fp32   same column order as Y
+ *   H_pre, H_post [B][n] fp32;  H_res [B][n][n] fp32, row i = output stream i
+ *
+ * Precision: bf16 inputs, fp32 accumulation, fp32 coefficients; bf16 outputs
+ * are rounded to nearest even.
+ *
+ * Ownership and ordering: every pointer is a DEVICE pointer owned by the
+ * caller; the library never allocates, frees or keeps a pointer after a call
+ * returns.  Each call only validates its arguments and enqueues kernels on
+ * `stream` (NULL = the legacy default stream); it returns without waiting.
+ *
+ * Argument rules (checked on the host; a failing call launches nothing):
+ *   - B >= 0; B == 0 is a no-op that returns MHC_OK;
+ *   - 1 <= n <= 8; C >= 8 and C % 8 == 0;  otherwise MHC_ERR_UNSUPPORTED;
+ *   - pointers non-NULL (MHC_ERR_INVALID) and 16-byte aligned (MHC_ERR_ALIGN);
+ *   - an output may not overlap any input or another output
+ *     (MHC_ERR_INVALID), except that X_next may be exactly X;
+ *   - iters >= 0 (MHC_ERR_INVALID);
+ *   - the current device must be compute capability 10.3 (sm_103,
+ *     GB300); otherwise MHC_ERR_UNSUPPORTED.
+ * Errors are returned as int status codes; no C++ exception crosses the ABI.
+ * Faults inside kernels surface as CUDA errors on the caller's next
+ * synchronisation; bounded waits that run out are reported by
+ * mhc_device_status().
+ */
+#ifndef MHC_H
+#define MHC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t mhc_bf16;          /* a bf16 value, stored as its 16-bit pattern */
+typedef struct CUstream_st *mhc_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+    MHC_OK = 0,
+    MHC_ERR_INVALID = -1,     /* bad size, NULL pointer, overlapping buffers, iters < 0 */
+    MHC_ERR_UNSUPPORTED = -2, /* n, C or device outside what the kernels handle */
+    MHC_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
+    MHC_ERR_CUDA = -4,        /* a CUDA runtime call or a kernel launch failed */
+    MHC_ERR_TIMEOUT = -5,     /* a bounded device wait ran out (see mhc_device_status) */
+    MHC_ERR_WORKSPACE = -6    /* workspace NULL or smaller than mhc_workspace_bytes() */
+} mhc_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *mhc_status_str(int status);
+
+/*
+ * Bytes of device workspace mhc_gemm_rms and mhc_forward need for (B, n, C)
+ * on the CURRENT device (the split-K partial sums and tile counters of §5.1's
+ * two-stage reduction).  Depends on the device's SM count.  Returns 0 when
+ * the arguments are out of range.  The workspace needs no initialisation
+ * and holds nothing between calls; calls that share one workspace must be
+ * ordered (same stream, or synchronised).
+ */
+size_t mhc_workspace_bytes(int64_t B, int n, int64_t C);
+
+/*
+ * Step 1 — GEMM fused with the RMS reduction (§2.1, §2.2; fusion §3.1).
+ *   Y[b][k] = Σ_{q<K} X[b][q]·φ[q][k]  (= Σ_q X[b][q]·phi_t[k][q]),  k < N
+ *   r[b]    = sqrt( Σ_{q<K} X[b][q]² / K )   (no epsilon)
+ * X is read from HBM once: the square-sum is taken from the same on-chip
+ * tiles that feed the tensor cores.  Results are bitwise reproducible for a
+ * given device and shape (fixed split-K summation order).  A token whose row
+ * is all zero gets r = 0 (its coefficients are then not finite).
+ */
+int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C,
+                 float *Y, float *r, void *workspace, size_t workspace_bytes,
+                 mhc_stream_t stream);
+
+/*
+ * Steps 2–3 — coefficients (§2.3, §2.4; fusions §3.2, §3.3).
+ *   H̃[b][k]   = α_seg·Y[b][k]/r[b] + bias[k]   (α_pre / α_post / α_res by column segment)
+ *   H_pre     = 1/(1+e^{-H̃_pre}),  H_post = 2/(1+e^{-H̃_post})
+ *   H_res     = Sinkhorn–Knopp: start from exp(H̃_res) as an n×n matrix, then
+ *               `iters` times divide each row by its sum, then each column
+ *               by its sum.  iters = 0 returns exp(H̃_res) unnormalised.
+ * The n×n iteration runs in registers, one token per thread.
+ */
+int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post,
+               float alpha_res, const float *bias, int iters, int64_t B, int n,
+               float *H_pre, float *H_post, float *H_res, mhc_stream_t stream);
+
+/*
+ * Step 4a — pre-mixing, n streams to one (§2.5 (1)):
+ *   F_pre[b][c] = Σ_{i<n} H_pre[b][i]·X[b][i][c]
+ */
+int mhc_pre_apply(const mhc_bf16 *X, const float *H_pre, int64_t B, int n, int64_t C,
+                  mhc_bf16 *F_pre, mhc_stream_t stream);
+
+/*
+ * Step 4b — residual and post mixing, fused (§2.5 (3), fusion §3.4):
+ *   X_next[b][i][c] = Σ_{j<n} H_res[b][i][j]·X[b][j][c] + H_post[b][i]·F_out[b][c]
+ * X is read once and X_next written once.  X_next may be exactly X (in-place
+ * update); any other overlap is rejected.
+ */
+int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_res,
+                       const float *H_post, int64_t B, int n, int64_t C, mhc_bf16 *X_next,
+                       mhc_stream_t stream);
+
+/*
+ * The whole forward: mhc_gemm_rms, mhc_coeffs, mhc_pre_apply and
+ * mhc_post_res_apply in that order on `stream`, with the same argument rules
+ * as the four calls.  F_out is an input: inside a real layer it is F(F_pre),
+ * which lies outside mHC (§2.5 (2)).  X_next may be exactly X.
+ */
+int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                void *workspace, size_t workspace_bytes, mhc_stream_t stream);
+
+/*
+ * Reads and clears the device status word of the current device: MHC_OK, or
+ * MHC_ERR_TIMEOUT when a bounded wait inside a kernel ran out since the last
+ * read (the kernel then stopped early, so its outputs are not valid).
+ * Blocks until all prior work on the device has finished.  Returns MHC_OK or
+ * MHC_ERR_CUDA; the status is written to *status.
+ */
+int mhc_device_status(int *status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHC_H */

@@ -1,0 +1,145 @@
+"""The C ABI without a GPU: the library loads, exports every call that
+include/mhc.h declares, and rejects bad arguments on the host before any
+device work.  Pointers here are fake addresses that are never dereferenced.
+"""
+import os
+import re
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mhc.h")
+
+mhc = pytest.importorskip("gemm_rms_sinkhorn_gb300")
+L = mhc._lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mhc_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls():
+    names = declared_functions()
+    for f in ("mhc_gemm_rms", "mhc_coeffs", "mhc_pre_apply", "mhc_post_res_apply", "mhc_forward"):
+        assert f in names
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", mhc.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (mhc_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, missing
+    for n in names:
+        assert hasattr(L, n)
+    assert set(names) <= set(mhc.EXPORTED)
+
+
+def test_status_strings():
+    for st in range(-6, 1):
+        s = mhc.mhc_status_str(st)
+        assert s.startswith("MHC_")
+    assert "unknown" in mhc.mhc_status_str(-99)
+
+
+# fake, 16-byte aligned, far-apart device addresses
+A, B_, C_, D, E, F, G, H, I, J, W = [0x10000000 * (k + 1) for k in range(11)]
+
+
+def gemm(X=A, phi=B_, Bt=4, n=4, C=256, Y=C_, r=D, ws=W, wsb=1 << 30):
+    return L.mhc_gemm_rms(X, phi, Bt, n, C, Y, r, ws, wsb, None)
+
+
+def coeffs(Y=A, r=B_, bias=C_, iters=20, Bt=4, n=4, hp=D, hq=E, hr=F):
+    return L.mhc_coeffs(Y, r, 0.01, 0.01, 0.01, bias, iters, Bt, n, hp, hq, hr, None)
+
+
+def pre(X=A, Hp=B_, Bt=4, n=4, C=256, Fp=C_):
+    return L.mhc_pre_apply(X, Hp, Bt, n, C, Fp, None)
+
+
+def post(X=A, Fo=B_, Hr=C_, Hq=D, Bt=4, n=4, C=256, Xn=E):
+    return L.mhc_post_res_apply(X, Fo, Hr, Hq, Bt, n, C, Xn, None)
+
+
+def fwd(X=A, phi=B_, Fo=C_, bias=D, iters=20, Bt=4, n=4, C=256, Y=E, r=F, hp=G, hq=H, hr=I,
+        Fp=J, Xn=0x1_0000_0000, ws=W, wsb=1 << 30):
+    return L.mhc_forward(X, phi, Fo, 0.01, 0.01, 0.01, bias, iters, Bt, n, C, Y, r, hp, hq, hr,
+                         Fp, Xn, ws, wsb, None)
+
+
+NO_DEVICE = mhc.MHC_ERR_CUDA  # valid host arguments reach the device check
+
+
+def test_empty_batch_is_a_noop():
+    assert gemm(Bt=0, X=None, phi=None, Y=None, r=None, ws=None, wsb=0) == mhc.MHC_OK
+    assert coeffs(Bt=0) == mhc.MHC_OK
+    assert pre(Bt=0) == mhc.MHC_OK
+    assert post(Bt=0) == mhc.MHC_OK
+    assert fwd(Bt=0) == mhc.MHC_OK
+
+
+@pytest.mark.parametrize("call", [gemm, pre, post, fwd])
+def test_shape_rules(call):
+    assert call(n=0) == mhc.MHC_ERR_UNSUPPORTED
+    assert call(n=9) == mhc.MHC_ERR_UNSUPPORTED
+    assert call(C=12) == mhc.MHC_ERR_UNSUPPORTED
+    assert call(C=0) == mhc.MHC_ERR_UNSUPPORTED
+    assert call(Bt=-1) == mhc.MHC_ERR_INVALID
+
+
+def test_coeffs_rules():
+    assert coeffs(n=9) == mhc.MHC_ERR_UNSUPPORTED
+    assert coeffs(iters=-1) == mhc.MHC_ERR_INVALID
+    assert fwd(iters=-1) == mhc.MHC_ERR_INVALID
+    assert coeffs(Y=None) == mhc.MHC_ERR_INVALID
+
+
+def test_null_and_alignment():
+    assert gemm(X=None) == mhc.MHC_ERR_INVALID
+    assert pre(Fp=None) == mhc.MHC_ERR_INVALID
+    assert post(Hr=None) == mhc.MHC_ERR_INVALID
+    assert fwd(bias=None) == mhc.MHC_ERR_INVALID
+    assert gemm(X=A + 8) == mhc.MHC_ERR_ALIGN
+    assert post(Xn=E + 4) == mhc.MHC_ERR_ALIGN
+    assert coeffs(hr=F + 4) == mhc.MHC_ERR_ALIGN
+
+
+def test_overlap_rules():
+    # an output over an input
+    assert gemm(Y=A + 64) == mhc.MHC_ERR_INVALID
+    assert pre(Fp=A + 256) == mhc.MHC_ERR_INVALID
+    # two outputs over each other
+    assert coeffs(hq=D + 16) == mhc.MHC_ERR_INVALID
+    # partial overlap of X_next and X is rejected, exact aliasing is accepted
+    assert post(Xn=A + 1024) == mhc.MHC_ERR_INVALID
+    assert post(Xn=A) == NO_DEVICE
+    assert fwd(Xn=A) == NO_DEVICE
+    assert fwd(Fp=A) == mhc.MHC_ERR_INVALID
+
+
+def test_valid_arguments_reach_the_device_check():
+    assert gemm() == NO_DEVICE
+    assert coeffs() == NO_DEVICE
+    assert pre() == NO_DEVICE
+    assert post() == NO_DEVICE
+    assert fwd() == NO_DEVICE
+    assert mhc.mhc_workspace_bytes(64, 4, 256) == 0  # needs a device
+    assert mhc.mhc_workspace_bytes(64, 9, 256) == 0
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """A copy of the package without libmhc_gb300.so must not import (no fallback)."""
+    import shutil
+    pkg = os.path.join(ROOT, "gemm_rms_sinkhorn_gb300")
+    dst = tmp_path / "gemm_rms_sinkhorn_gb300"
+    shutil.copytree(pkg, dst, ignore=shutil.ignore_patterns("*.so", "_build", "__pycache__"))
+    code = "import gemm_rms_sinkhorn_gb300"
+    res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True,
+                         text=True)
+    assert res.returncode != 0 and "ImportError" in res.stderr

@@ -1,0 +1,74 @@
+"""Host logic of bench.py on CPU: byte accounting, the reference arm, and the
+N > 1 rank combination over a 2-process gloo group."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_prefill():
+    """Compulsory bytes per kernel at B=16384, n=4, C=7168 (X read once, outputs written once)."""
+    a = bench.algorithmic_bytes(16384, 4, 7168)
+    assert a["gemm_rms"] == 942_538_752
+    assert a["coeffs"] == 3_211_360
+    assert a["pre_apply"] == 1_174_667_264
+    assert a["post_res_apply"] == 2_115_239_936
+    assert sum(a.values()) == 4_235_657_312
+
+
+def test_tokens_per_second_is_whole_job():
+    assert bench.tokens_per_second(16384, 4, 10, 1000.0) == 16384 * 4 * 10
+    assert bench.max_over_ranks(3.5) == 3.5
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [120.0, 150.0][rank]  # rank 1 is the slower one
+    worst = bench.max_over_ranks(ms, dist, torch.device("cpu"))
+    q.put((rank, worst, bench.tokens_per_second(1000, world, 5, worst)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_rank_combination_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + (os.getpid() % 1000)
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [g[1] for g in got] == [150.0, 150.0]
+    assert got[0][2] == pytest.approx(1000 * 2 * 5 / 0.150)
+
+
+def test_reference_arm_on_cpu():
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "2", "--warmup", "1", "--ref-tokens", "4"],
+                         capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr
+    line = json.loads(res.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_are_silent():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2")
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                         env=env, timeout=120)
+    assert res.returncode == 0 and res.stdout.strip() == ""

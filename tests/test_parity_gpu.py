@@ -1,0 +1,308 @@
+"""GPU parity: every kernel of the library, through the C ABI, against the
+fp64 oracle on the same seeded inputs (page "mHC 算法分析 & cutile 高效实现",
+§2.1–§2.5).  Tolerances are in ``gpu_util``.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (H_TOL, R_REL, assert_abs, assert_bf16_close, assert_rel, assert_Y_close,
+                      cuda_ok, dev_bf16, dev_f32, f64, host64, host_bits, phi_KN, sample_rows)
+from synth import WORKLOADS, make_inputs
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA device")]
+
+mhc = pytest.importorskip("gemm_rms_sinkhorn_gb300")
+
+# (B, n, C): ragged tiles (B % 128 != 0), ragged K blocks (n*C % 64 != 0), every N padding
+ODD_SHAPES = [(1, 1, 8), (3, 2, 8), (5, 4, 16), (65, 5, 264), (129, 6, 40), (257, 7, 8),
+              (200, 4, 264), (130, 8, 72), (3, 3, 24)]
+
+
+def gemm_gpu(X_bits, phi_t_bits, n, C):
+    B = X_bits.shape[0]
+    N = n * n + 2 * n
+    Y = torch.empty(B, N, dtype=torch.float32, device="cuda")
+    r = torch.empty(B, dtype=torch.float32, device="cuda")
+    ws = mhc.workspace(B, n, C)
+    mhc.mhc_gemm_rms(dev_bf16(X_bits), dev_bf16(phi_t_bits), B, n, C, Y, r, ws)
+    torch.cuda.synchronize()
+    return host64(Y), host64(r)
+
+
+# ------------------------------------------------------------- step 1
+
+
+@pytest.mark.parametrize("B,n,C", ODD_SHAPES + [(1, 4, 7168), (128, 4, 7168), (300, 8, 512)])
+def test_gemm_rms_exact_integers(B, n, C):
+    """Integer X, φ in [-2, 2]: Ỹ and Σx² are exact in fp32, so Y must match bit for bit."""
+    K, N = n * C, n * n + 2 * n
+    X = synth.int_bf16((B, K), 101, 0, -2, 2)
+    phi_t = synth.int_bf16((N, K), 101, 2, -2, 2)
+    Y, r = gemm_gpu(X, phi_t, n, C)
+    Yr, rr = oracle.gemm_rms(X, phi_KN(phi_t), n, C)
+    assert np.array_equal(Y, Yr), "max |dY| %g" % np.max(np.abs(Y - Yr))
+    assert_rel(r, rr, 2.0 ** -22, "r (1 ulp)")
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode8", "decode32", "decode128", "7b"])
+def test_gemm_rms_workloads(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, seed=0, parts=("X", "phi_t"))
+    Y, r = gemm_gpu(inp["X"], inp["phi_t"], wl.n, wl.C)
+    Yr, rr = oracle.gemm_rms(inp["X"], phi_KN(inp["phi_t"]), wl.n, wl.C)
+    assert_Y_close(Y, Yr, inp["X"], inp["phi_t"])
+    assert_rel(r, rr, R_REL, "r")
+
+
+@pytest.mark.parametrize("B,n,C", ODD_SHAPES)
+def test_gemm_rms_odd_shapes(B, n, C):
+    K, N = n * C, n * n + 2 * n
+    X = synth.normal_bf16((B, K), 7, 0)
+    phi_t = synth.normal_bf16((N, K), 7, 2, 0.02)
+    Y, r = gemm_gpu(X, phi_t, n, C)
+    Yr, rr = oracle.gemm_rms(X, phi_KN(phi_t), n, C)
+    assert_Y_close(Y, Yr, X, phi_t)
+    assert_rel(r, rr, R_REL, "r")
+
+
+def test_gemm_rms_deterministic():
+    wl = WORKLOADS["decode32"]
+    inp = make_inputs(wl, seed=1, parts=("X", "phi_t"))
+    a = gemm_gpu(inp["X"], inp["phi_t"], wl.n, wl.C)
+    b = gemm_gpu(inp["X"], inp["phi_t"], wl.n, wl.C)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------- steps 2-3
+
+
+def coeffs_gpu(Y, r, al, bias, iters, n):
+    B = Y.shape[0]
+    Hp = torch.empty(B, n, device="cuda")
+    Hq = torch.empty(B, n, device="cuda")
+    Hr = torch.empty(B, n, n, device="cuda")
+    mhc.mhc_coeffs(dev_f32(Y), dev_f32(r), al[0], al[1], al[2], dev_f32(bias), iters, B, n,
+                   Hp, Hq, Hr)
+    torch.cuda.synchronize()
+    return host64(Hp), host64(Hq), host64(Hr)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("iters", [0, 1, 5, 20, 50])
+def test_coeffs(n, iters):
+    B, N = 300, n * n + 2 * n
+    Y = synth.normal_f32((B, N), 200 + n, 9, 3.0)
+    r = np.abs(synth.normal_f32(B, 300 + n, 9, 1.0)) + 0.05
+    bias = synth.normal_f32(N, 400 + n, 3, 0.5)
+    al = (0.7, -0.3, 0.9)
+    Hp, Hq, Hr = coeffs_gpu(Y, r, al, bias, iters, n)
+    # the oracle gets the very same fp32 values, widened
+    Op, Oq, Or = oracle.coeffs(Y.astype(np.float64), r.astype(np.float64), np.float32(al[0]),
+                               np.float32(al[1]), np.float32(al[2]), bias.astype(np.float64),
+                               iters)
+    assert_abs(Hp, Op, H_TOL, "H_pre")
+    assert_abs(Hq, Oq, H_TOL, "H_post")
+    # |H̃| reaches ~100 here, where σ rounds to exactly 0 or 1: closed ranges
+    assert (Hp >= 0).all() and (Hp <= 1).all() and (Hq >= 0).all() and (Hq <= 2).all()
+    if iters == 0:
+        # raw exp(H̃_res): relative agreement in fp32's normal range; below it
+        # (H̃ < -87) fp32 underflows to a denormal or zero
+        normal = Or >= 1e-30
+        assert_rel(Hr[normal], Or[normal], 1e-5, "exp(H̃_res)")
+        assert (Hr[~normal] <= 1e-29).all()
+    else:
+        assert_abs(Hr, Or, H_TOL, "H_res")
+        assert_abs(Hr.sum(axis=1), np.ones((B, n)), 1e-5, "H_res column sums")
+
+
+def test_coeffs_closed_forms():
+    """α = 0: H_pre = σ(b), H_post = 2σ(b), and a constant res bias gives H_res = 1/n."""
+    n, B = 4, 70
+    N = n * n + 2 * n
+    bias = np.zeros(N, dtype=np.float32)
+    bias[:n] = np.log(3.0)
+    bias[n:2 * n] = -np.log(3.0)
+    bias[2 * n:] = 0.25
+    Y = synth.normal_f32((B, N), 5, 9, 1.0)
+    r = np.ones(B, dtype=np.float32)
+    Hp, Hq, Hr = coeffs_gpu(Y, r, (0.0, 0.0, 0.0), bias, 20, n)
+    assert_abs(Hp, np.full((B, n), 0.75), 1e-6, "σ(ln 3)")
+    assert_abs(Hq, np.full((B, n), 0.5), 1e-6, "2σ(-ln 3)")
+    assert_abs(Hr, np.full((B, n, n), 0.25), 1e-6, "1/n")
+
+
+# ------------------------------------------------------------- step 4
+
+
+@pytest.mark.parametrize("B,n,C", ODD_SHAPES + [(64, 4, 7168)])
+def test_pre_apply(B, n, C):
+    X = synth.normal_bf16((B, n * C), 11, 0)
+    Hp = np.abs(synth.normal_f32((B, n), 12, 9, 0.5)) % 1.0
+    F = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+    mhc.mhc_pre_apply(dev_bf16(X), dev_f32(Hp), B, n, C, F)
+    torch.cuda.synchronize()
+    assert_bf16_close(host64(F), oracle.pre_apply(X, Hp.astype(np.float64), n, C), "F_pre")
+
+
+def test_pre_apply_onehot_is_exact():
+    B, n, C = 9, 4, 136
+    X = synth.normal_bf16((B, n * C), 13, 0)
+    for i in range(n):
+        Hp = np.zeros((B, n), dtype=np.float32)
+        Hp[:, i] = 1.0
+        F = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+        mhc.mhc_pre_apply(dev_bf16(X), dev_f32(Hp), B, n, C, F)
+        torch.cuda.synchronize()
+        assert np.array_equal(host_bits(F), X.reshape(B, n, C)[:, i, :])
+
+
+def post_gpu(X, Fo, Hr, Hq, n, C, inplace=False):
+    B = Fo.shape[0]
+    Xd = dev_bf16(X)
+    out = Xd if inplace else torch.empty_like(Xd)
+    mhc.mhc_post_res_apply(Xd, dev_bf16(Fo), dev_f32(Hr), dev_f32(Hq), B, n, C, out)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("B,n,C", ODD_SHAPES + [(64, 4, 7168)])
+@pytest.mark.parametrize("inplace", [False, True])
+def test_post_res_apply(B, n, C, inplace):
+    X = synth.normal_bf16((B, n * C), 21, 0)
+    Fo = synth.normal_bf16((B, C), 21, 1)
+    Hr = oracle.sinkhorn(synth.normal_f32((B, n, n), 22, 9, 1.0), 20).astype(np.float32)
+    Hq = 2.0 * (np.abs(synth.normal_f32((B, n), 23, 9, 0.5)) % 1.0)
+    out = post_gpu(X, Fo, Hr, Hq, n, C, inplace)
+    ref = oracle.post_res_apply(X, Fo, Hr.astype(np.float64), Hq.astype(np.float64), n, C)
+    assert_bf16_close(host64(out), ref, "X_next")
+
+
+def test_post_res_apply_permutation_is_exact():
+    B, n, C = 5, 3, 64
+    X = synth.normal_bf16((B, n * C), 24, 0)
+    Fo = synth.normal_bf16((B, C), 24, 1)
+    pi = [2, 0, 1]
+    Hr = np.zeros((B, n, n), dtype=np.float32)
+    for i in range(n):
+        Hr[:, i, pi[i]] = 1.0
+    out = post_gpu(X, Fo, Hr, np.zeros((B, n), dtype=np.float32), n, C)
+    assert np.array_equal(host_bits(out).reshape(B, n, C), X.reshape(B, n, C)[:, pi, :])
+
+
+# ------------------------------------------------------------ forward
+
+
+def forward_gpu(inp, wl, inplace=False):
+    X = dev_bf16(inp["X"])
+    B = X.shape[0]
+    out = mhc.alloc_outputs(B, wl.n, wl.C)
+    if inplace:
+        out["X_next"] = X
+    mhc.forward(X, dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), wl.alpha_pre, wl.alpha_post,
+                wl.alpha_res, dev_f32(inp["bias"]), wl.iters, wl.n, wl.C, out=out)
+    torch.cuda.synchronize()
+    return out
+
+
+def check_forward(out, inp, wl, rows=None):
+    sel = slice(None) if rows is None else torch.as_tensor(rows, device="cuda")
+    X = inp["X"] if rows is None else inp["X"][rows]
+    Fo = inp["F_out"] if rows is None else inp["F_out"][rows]
+    ref = oracle.forward(X, phi_KN(inp["phi_t"]), Fo, wl.n, wl.C, wl.alpha_pre, wl.alpha_post,
+                         wl.alpha_res, inp["bias"], wl.iters)
+    g = {k: host64(out[k][sel]) for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre",
+                                           "X_next")}
+    assert_Y_close(g["Y"], ref["Y"], X, inp["phi_t"])
+    assert_rel(g["r"], ref["r"], R_REL, "r")
+    assert_abs(g["H_pre"], ref["H_pre"], H_TOL, "H_pre")
+    assert_abs(g["H_post"], ref["H_post"], H_TOL, "H_post")
+    assert_abs(g["H_res"], ref["H_res"], H_TOL, "H_res")
+    assert_bf16_close(g["F_pre"], ref["F_pre"], "F_pre")
+    assert_bf16_close(g["X_next"], ref["X_next"], "X_next")
+
+
+def check_properties(out, wl):
+    """Facts that hold at any size: ranges, Sinkhorn column sums, finite outputs."""
+    Hp, Hq, Hr = out["H_pre"], out["H_post"], out["H_res"]
+    assert bool(((Hp > 0) & (Hp < 1)).all()) and bool(((Hq > 0) & (Hq < 2)).all())
+    if wl.iters > 0:
+        colsum = Hr.double().sum(dim=1)
+        assert float((colsum - 1).abs().max()) <= 1e-5
+    assert bool(torch.isfinite(out["r"]).all()) and bool((out["r"] > 0).all())
+    for k in ("F_pre", "X_next"):
+        assert bool(torch.isfinite(out[k].float()).all())
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode8", "decode32", "decode128", "7b"])
+def test_forward_full_oracle(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, seed=0)
+    out = forward_gpu(inp, wl)
+    check_forward(out, inp, wl)
+    check_properties(out, wl)
+
+
+@pytest.mark.parametrize("name", ["wider_it5", "wider", "wider_it50"])
+def test_forward_wider_sampled(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, seed=0)
+    out = forward_gpu(inp, wl)
+    check_forward(out, inp, wl, rows=sample_rows(wl.B, 40))
+    check_properties(out, wl)
+
+
+def test_forward_prefill_full_size_sampled():
+    """B=16384, n=4, C=7168 in the launch configuration the benchmark times."""
+    wl = WORKLOADS["prefill"]
+    inp = make_inputs(wl, seed=0)
+    out = forward_gpu(inp, wl)
+    check_forward(out, inp, wl, rows=sample_rows(wl.B, 48))
+    check_properties(out, wl)
+    # run again: bitwise identical (fixed split-K order)
+    Y0, X0 = out["Y"].clone(), out["X_next"].clone()
+    out2 = forward_gpu(inp, wl)
+    assert torch.equal(Y0, out2["Y"]) and torch.equal(X0, out2["X_next"])
+
+
+@pytest.mark.parametrize("B,n,C", ODD_SHAPES)
+def test_forward_odd_shapes(B, n, C):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=3)
+    check_forward(forward_gpu(inp, wl), inp, wl)
+
+
+def test_forward_in_place():
+    wl = WORKLOADS["tiny"]
+    inp = make_inputs(wl, seed=4)
+    ref_out = forward_gpu(inp, wl)
+    out = forward_gpu(inp, wl, inplace=True)
+    assert torch.equal(out["X_next"], ref_out["X_next"])
+    check_forward(out, inp, wl)
+
+
+def test_forward_empty_batch_is_a_noop():
+    wl = WORKLOADS["tiny"]
+    e = torch.empty(0, wl.n * wl.C, dtype=torch.bfloat16, device="cuda")
+    phi = torch.zeros(wl.N, wl.K, dtype=torch.bfloat16, device="cuda")
+    out = mhc.alloc_outputs(0, wl.n, wl.C)
+    mhc.forward(e, phi, torch.empty(0, wl.C, dtype=torch.bfloat16, device="cuda"), 0.01, 0.01,
+                0.01, torch.zeros(wl.N, device="cuda"), 20, wl.n, wl.C, out=out)
+
+
+def test_workspace_too_small_is_rejected():
+    wl = WORKLOADS["tiny"]
+    inp = make_inputs(wl, seed=0)
+    out = mhc.alloc_outputs(wl.B, wl.n, wl.C)
+    out["ws"] = out["ws"][:16]
+    with pytest.raises(mhc.MhcError) as ei:
+        mhc.forward(dev_bf16(inp["X"]), dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), 0.01,
+                    0.01, 0.01, dev_f32(inp["bias"]), 20, wl.n, wl.C, out=out)
+    assert ei.value.status == mhc.MHC_ERR_WORKSPACE
+
+
+def test_device_status_is_clean():
+    assert mhc.mhc_device_status() == mhc.MHC_OK
