@@ -3,7 +3,7 @@
 Argument marshalling only: every step of the mHC forward runs in the CUDA
 kernels of ``libmhc_gb300.so``.  PyTorch supplies device memory and streams.
 Importing this package raises ``ImportError`` when the library has not been
-built (``python -m gemm_rms_sinkhorn_gb300.build``); there is no fallback.
+built (``python gemm_rms_sinkhorn_gb300/build.py``); there is no fallback.
 
 Functions carry the C names and take torch tensors in the layouts of
 ``mhc.h`` (bf16 tensors as ``torch.bfloat16``, fp32 as ``torch.float32``, all
@@ -21,7 +21,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmhc_gb300.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("%s is missing: build it with `python -m gemm_rms_sinkhorn_gb300.build` "
+    raise ImportError("%s is missing: build it with `python gemm_rms_sinkhorn_gb300/build.py` "
                       "(or __graft_entry__.build())" % LIB_PATH)
 
 _lib = ctypes.CDLL(LIB_PATH)
@@ -46,6 +46,7 @@ _SIGS = {
     "mhc_forward": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
+    "mhc_gemm_rms_noalloc": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -153,6 +154,16 @@ def mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, 
                             _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
                             _stream(stream)),
            "mhc_forward")
+
+
+def mhc_gemm_rms_noalloc(X, phi_t, B, n, C, Y, r, stream=None):
+    """mhc_gemm_rms with the library's built-in scratch: for callers that cannot
+    allocate device memory (no workspace argument; calls on one device must not
+    overlap on the GPU)."""
+    bf, f = torch.bfloat16, torch.float32
+    _check(_lib.mhc_gemm_rms_noalloc(_ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), B, n, C,
+                                     _ptr(Y, f, "Y"), _ptr(r, f, "r"), _stream(stream)),
+           "mhc_gemm_rms_noalloc")
 
 
 def mhc_device_status() -> int:

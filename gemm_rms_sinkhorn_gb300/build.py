@@ -3,7 +3,7 @@
 Each ``csrc/*.cu`` file is compiled by its own ``nvcc`` process (in parallel)
 with ``-gencode arch=compute_103a,code=sm_103a``, then the objects are linked
 into one shared library next to this file.  Only sources newer than their
-object are recompiled.  Run ``python -m gemm_rms_sinkhorn_gb300.build``.
+object are recompiled.  Run ``python gemm_rms_sinkhorn_gb300/build.py``.
 """
 from __future__ import annotations
 

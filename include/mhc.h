@@ -141,6 +141,39 @@ int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
                 void *workspace, size_t workspace_bytes, mhc_stream_t stream);
 
 /*
+ * Size of the built-in scratch array of mhc_gemm_rms_noalloc: 16 MiB, held in
+ * device memory by every GPU that loads this library, until the process
+ * exits.  A (B, n, C) fits when mhc_workspace_bytes(B, n, C) is at most this
+ * (on a 152-SM GB300 the scratch does not depend on C: n=4 fits up to
+ * B = 148,224 tokens, n=8 up to B = 32,256).
+ */
+#define MHC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * mhc_gemm_rms without a workspace argument: the same computation, kernel and
+ * results, with the split-K scratch taken from the library's own fixed device
+ * array instead of caller memory.  The mHC page has no counterpart to this
+ * call; it exists for callers that cannot allocate device memory where they
+ * call it — code running inside a host framework that owns all device memory
+ * through its own pool, or a latency-critical path where a cudaMalloc (which
+ * can synchronise the device) is not acceptable.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * - Same argument rules and status codes as mhc_gemm_rms.  A problem that
+ *   needs more than MHC_NOALLOC_SCRATCH_BYTES of scratch is rejected with
+ *   MHC_ERR_WORKSPACE before anything is launched.
+ * - The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any
+ *   stream capture on that device.
+ * - Every call on a device shares the one array and it keeps the last call's
+ *   contents (each call clears what must start at zero itself).  Calls that
+ *   overlap on the GPU — on different streams, or from different threads
+ *   without ordering — race on it: order them.
+ */
+int mhc_gemm_rms_noalloc(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C,
+                         float *Y, float *r, mhc_stream_t stream);
+
+/*
  * Reads and clears the device status word of the current device: MHC_OK, or
  * MHC_ERR_TIMEOUT when a bounded wait inside a kernel ran out since the last
  * read (the kernel then stopped early, so its outputs are not valid).
