@@ -245,6 +245,33 @@ def tokens_per_second(tokens_per_rank: int, world: int, steps: int, ms_total: fl
 # ------------------------------------------------------------------ GPU arm
 
 
+def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out) -> dict:
+    """Mean CUDA-event time (ms) of each kernel over `steps` passes of the four
+    entry points, events recorded between launches on the launching stream."""
+    import torch
+
+    B, n, C = wl.B, wl.n, wl.C
+    nk = len(KERNELS)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)] for _ in range(steps)]
+    barrier()
+    for s in range(steps):
+        e = evs[s]
+        e[0].record(stream)
+        mhc.mhc_gemm_rms(X, phi_t, B, n, C, out["Y"], out["r"], out["ws"], stream)
+        e[1].record(stream)
+        mhc.mhc_coeffs(out["Y"], out["r"], wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                       wl.iters, B, n, out["H_pre"], out["H_post"], out["H_res"], stream)
+        e[2].record(stream)
+        mhc.mhc_pre_apply(X, out["H_pre"], B, n, C, out["F_pre"], stream)
+        e[3].record(stream)
+        mhc.mhc_post_res_apply(X, F_out, out["H_res"], out["H_post"], B, n, C, out["X_next"],
+                               stream)
+        e[4].record(stream)
+    barrier()
+    return {k: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps))
+            for i, k in enumerate(KERNELS)}
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -257,6 +284,10 @@ def main() -> int:
     ap.add_argument("--ref-tokens", type=int, default=128,
                     help="tokens per step of the --impl reference arm")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of identical load kept up for the clock samples")
+    ap.add_argument("--mode", default="full", choices=["full", "kernels"],
+                    help="kernels: only the per-kernel loop (small runs for ncu captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -314,6 +345,18 @@ def main() -> int:
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
 
+    if args.mode == "kernels":
+        for _ in range(args.warmup):
+            step()
+        barrier()
+        ms = per_kernel_times(mhc, stream, barrier, args.steps, wl, X, phi_t, F_out, bias, out)
+        sampler.stop()
+        if dist is not None:
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps({"mode": "kernels", "workload": wl.name, "ms": ms}), flush=True)
+        return 0
+
     # ---- timed region: K whole forward steps
     for _ in range(args.warmup):
         step()
@@ -329,7 +372,7 @@ def main() -> int:
     # keep the same load up for ~1 s when the timed region is short, so the
     # clock samples describe the loaded state of the timed steps
     t_host1 = time.time()
-    extra_until = t_host0 + 1.0
+    extra_until = t_host0 + args.clock_window
     while time.time() < extra_until:
         for _ in range(20):
             step()
@@ -340,27 +383,8 @@ def main() -> int:
     value = tokens_per_second(B, world, args.steps, ms_total)
 
     # ---- per-kernel CUDA-event times over the same steps (same stream)
-    nk = len(KERNELS)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-           for _ in range(args.steps)]
-    barrier()
-    for s in range(args.steps):
-        e = evs[s]
-        e[0].record(stream)
-        mhc.mhc_gemm_rms(X, phi_t, B, n, C, out["Y"], out["r"], out["ws"], stream)
-        e[1].record(stream)
-        mhc.mhc_coeffs(out["Y"], out["r"], wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
-                       wl.iters, B, n, out["H_pre"], out["H_post"], out["H_res"], stream)
-        e[2].record(stream)
-        mhc.mhc_pre_apply(X, out["H_pre"], B, n, C, out["F_pre"], stream)
-        e[3].record(stream)
-        mhc.mhc_post_res_apply(X, F_out, out["H_res"], out["H_post"], B, n, C, out["X_next"],
-                               stream)
-        e[4].record(stream)
-    barrier()
-    per_kernel_ms = {k: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1])
-                                         for s in range(args.steps))
-                     for i, k in enumerate(KERNELS)}
+    per_kernel_ms = per_kernel_times(mhc, stream, barrier, args.steps, wl, X, phi_t, F_out, bias,
+                                     out)
     sampler.stop()
     status = mhc.mhc_device_status()
     if status != mhc.MHC_OK:
