@@ -6,10 +6,14 @@
 //   H̃ = α_seg·Y/r + b;  H_pre = σ(H̃_pre);  H_post = 2σ(H̃_post)
 //   H_res = exp(H̃_res), then `iters` × (rows /= row sums; columns /= column sums)
 //
-// One thread owns one token: its n×n block lives in registers for all
-// iterations.  Y rows are staged through shared memory so global loads and
-// stores stay coalesced; the N = n²+2n outputs of a token overwrite its own
-// Y row in shared memory and leave in three coalesced streams.
+// A token is handled by a group of n consecutive lanes of a warp; lane i of
+// the group owns row i of the n×n block (in registers) and entry i of the pre
+// and post segments.  Row sums are lane-local; column sums are a shuffle
+// reduction across the group that every lane evaluates in the same order, so
+// all lanes divide a column by the identical sum.  Each normalisation takes
+// one correctly rounded reciprocal per sum and multiplies by it (at most one
+// rounding away from a true division).  Spreading a token over n lanes gives
+// the serial iteration n times more warps to hide its latency.
 //
 // Before the first row normalisation each row is shifted by its maximum:
 // exp(h - m)/Σ exp(h - m) = exp(h)/Σ exp(h), so every iterate from the first
@@ -24,90 +28,87 @@
 namespace mhc {
 namespace {
 
-constexpr int kTokensPerBlock = 128;
+constexpr int kThreads = 128;
+
+// Sum over the n lanes of a token group of v, identical on every lane.
+template <int n>
+__device__ __forceinline__ float group_sum(float v, int base, unsigned mask)
+{
+    if constexpr ((n & (n - 1)) == 0) {
+        // butterfly: a + b == b + a exactly, so every lane ends with the same value
+#pragma unroll
+        for (int off = 1; off < n; off <<= 1) v += __shfl_xor_sync(mask, v, off);
+        return v;
+    } else {
+        float s = __shfl_sync(mask, v, base);
+#pragma unroll
+        for (int k = 1; k < n; ++k) s += __shfl_sync(mask, v, base + k);
+        return s;
+    }
+}
 
 template <int n>
-__global__ void __launch_bounds__(kTokensPerBlock)
+__global__ void __launch_bounds__(kThreads)
 coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_pre, float a_post,
               float a_res, const float *__restrict__ bias, int iters, int64_t B,
               float *__restrict__ H_pre, float *__restrict__ H_post, float *__restrict__ H_res)
 {
     constexpr int N = n * n + 2 * n;
-    __shared__ float rows_s[kTokensPerBlock * N];
-    __shared__ float bias_s[N];
+    constexpr int kGroups = 32 / n;  // tokens per warp
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int g = lane / n;          // token group within the warp
+    const int i = lane - g * n;      // row owned by this lane
+    const int base = g * n;
+    // lanes of whole groups take part in the shuffles; the spare lanes
+    // (32 mod n of them) sit out
+    const unsigned mask = kGroups * n == 32 ? 0xFFFFFFFFu : ((1u << (kGroups * n)) - 1u);
+    if (g >= kGroups) return;
 
-    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * kTokensPerBlock;
-    const int rows = static_cast<int>(B - b0 < kTokensPerBlock ? B - b0 : kTokensPerBlock);
-    for (int i = threadIdx.x; i < rows * N; i += kTokensPerBlock) rows_s[i] = Y[b0 * N + i];
-    if (threadIdx.x < N) bias_s[threadIdx.x] = bias[threadIdx.x];
-    __syncthreads();
+    const int64_t t = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kGroups + g;
+    const bool valid = t < B;
+    const int64_t tt = valid ? t : B - 1;  // idle groups mirror the last token, store nothing
+    const float *y = Y + tt * N;
+    const float rb = __ldg(r + tt);
 
-    if (threadIdx.x < rows) {
-        float *h = rows_s + threadIdx.x * N;
-        const float rb = r[b0 + threadIdx.x];
-        // §2.3 + §2.4 for the pre and post segments
+    // §2.3 + §2.4, pre and post entries i
+    const float tp = a_pre * __ldg(y + i) / rb + __ldg(bias + i);
+    const float tq = a_post * __ldg(y + n + i) / rb + __ldg(bias + n + i);
+    const float hp = 1.0f / (1.0f + expf(-tp));
+    const float hq = 2.0f / (1.0f + expf(-tq));
+
+    // §2.4 Sinkhorn–Knopp, row i of the res block
+    float m[n];
 #pragma unroll
-        for (int i = 0; i < n; ++i) {
-            const float tp = a_pre * h[i] / rb + bias_s[i];
-            const float tq = a_post * h[n + i] / rb + bias_s[n + i];
-            h[i] = 1.0f / (1.0f + expf(-tp));
-            h[n + i] = 2.0f / (1.0f + expf(-tq));
-        }
-        // §2.4 Sinkhorn–Knopp on the res segment
-        float m[n][n];
+    for (int j = 0; j < n; ++j)
+        m[j] = a_res * __ldg(y + 2 * n + i * n + j) / rb + __ldg(bias + 2 * n + i * n + j);
+    if (iters > 0) {
+        float mx = m[0];
 #pragma unroll
-        for (int i = 0; i < n; ++i)
+        for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[j]);
 #pragma unroll
-            for (int j = 0; j < n; ++j)
-                m[i][j] = a_res * h[2 * n + i * n + j] / rb + bias_s[2 * n + i * n + j];
-        if (iters > 0) {
+        for (int j = 0; j < n; ++j) m[j] = expf(m[j] - mx);
+    } else {
 #pragma unroll
-            for (int i = 0; i < n; ++i) {
-                float mx = m[i][0];
-#pragma unroll
-                for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[i][j]);
-#pragma unroll
-                for (int j = 0; j < n; ++j) m[i][j] = expf(m[i][j] - mx);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < n; ++i)
-#pragma unroll
-                for (int j = 0; j < n; ++j) m[i][j] = expf(m[i][j]);
-        }
-        for (int t = 0; t < iters; ++t) {
-#pragma unroll
-            for (int i = 0; i < n; ++i) {
-                float s = 0.f;
-#pragma unroll
-                for (int j = 0; j < n; ++j) s += m[i][j];
-#pragma unroll
-                for (int j = 0; j < n; ++j) m[i][j] = m[i][j] / s;
-            }
-#pragma unroll
-            for (int j = 0; j < n; ++j) {
-                float s = 0.f;
-#pragma unroll
-                for (int i = 0; i < n; ++i) s += m[i][j];
-#pragma unroll
-                for (int i = 0; i < n; ++i) m[i][j] = m[i][j] / s;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < n; ++i)
-#pragma unroll
-            for (int j = 0; j < n; ++j) h[2 * n + i * n + j] = m[i][j];
+        for (int j = 0; j < n; ++j) m[j] = expf(m[j]);
     }
-    __syncthreads();
-
-    for (int e = threadIdx.x; e < rows * n; e += kTokensPerBlock) {
-        const int t = e / n, i = e - t * n;
-        H_pre[b0 * n + e] = rows_s[t * N + i];
-        H_post[b0 * n + e] = rows_s[t * N + n + i];
+    for (int it = 0; it < iters; ++it) {
+        float s = m[0];
+#pragma unroll
+        for (int j = 1; j < n; ++j) s += m[j];
+        const float inv = __frcp_rn(s);
+#pragma unroll
+        for (int j = 0; j < n; ++j) m[j] *= inv;
+#pragma unroll
+        for (int j = 0; j < n; ++j) m[j] *= __frcp_rn(group_sum<n>(m[j], base, mask));
     }
-    for (int e = threadIdx.x; e < rows * n * n; e += kTokensPerBlock) {
-        const int t = e / (n * n), ij = e - t * (n * n);
-        H_res[b0 * n * n + e] = rows_s[t * N + 2 * n + ij];
+
+    if (valid) {
+        H_pre[t * n + i] = hp;
+        H_post[t * n + i] = hq;
+        float *o = H_res + t * n * n + i * n;
+#pragma unroll
+        for (int j = 0; j < n; ++j) o[j] = m[j];
     }
 }
 
@@ -116,8 +117,9 @@ cudaError_t launch_n(const float *Y, const float *r, float a_pre, float a_post, 
                      const float *bias, int iters, int64_t B, float *H_pre, float *H_post,
                      float *H_res, cudaStream_t stream)
 {
-    const int64_t blocks = (B + kTokensPerBlock - 1) / kTokensPerBlock;
-    coeffs_kernel<n><<<static_cast<unsigned>(blocks), kTokensPerBlock, 0, stream>>>(
+    constexpr int64_t tokens_per_block = (kThreads / 32) * (32 / n);
+    const int64_t blocks = (B + tokens_per_block - 1) / tokens_per_block;
+    coeffs_kernel<n><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
         Y, r, a_pre, a_post, a_res, bias, iters, B, H_pre, H_post, H_res);
     return cudaGetLastError();
 }

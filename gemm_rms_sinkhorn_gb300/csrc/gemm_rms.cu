@@ -5,7 +5,8 @@
 //   Y[b][k] = Σ_q X[b][q]·φ[q][k]    r[b] = sqrt(Σ_q X[b][q]² / K)
 //
 // Design (sm_103a):
-//   * Work unit = one 128-token × 64-K block.  Units are ordered tile-major
+//   * Work unit = one 128-token × (64·KB)-K block, one pipeline stage of KB
+//     consecutive 64-column boxes (KB = kKB).  Units are ordered tile-major
 //     (all K blocks of token tile 0, then tile 1, ...) and split into equal
 //     contiguous ranges, one per persistent CTA (stream-K), so every SM gets
 //     the same number of units whatever B and K are.  N is tiny (24 or 80),
@@ -14,8 +15,10 @@
 //     multi-stage mbarrier ring.  Warp 1 issues tcgen05.mma (M=128,
 //     N=NPAD, K=16, bf16 in, fp32 accumulate) into a double-buffered TMEM
 //     accumulator.  Warps 2-5 sum x² for their 32 rows straight from the same
-//     shared-memory tiles (X is read from HBM once) and run the epilogue
-//     (tcgen05.ld of the accumulator).
+//     shared-memory tiles (X is read from HBM once) and hand each segment's
+//     sums over through a double-buffered shared slot.  Warps 6-9 run the
+//     epilogue (tcgen05.ld of the accumulator, partial sums, the fixed-order
+//     reduction), so the stage consumers never wait on epilogue work.
 //   * A tile covered by several CTAs is finished by the last one to arrive
 //     (atomic ticket): it adds the partial sums in contributor order, so
 //     the result is bitwise reproducible (§5.2 sums the splits in a fixed
@@ -35,29 +38,36 @@ namespace mhc {
 namespace {
 
 constexpr int kBM = 128;       // tokens per tile (MMA M)
-constexpr int kBK = 64;        // K elements per stage: one 128-byte swizzle row
-constexpr int kThreads = 192;  // 6 warps: TMA, MMA, 4 × square-sum/epilogue
+constexpr int kBK = 64;        // K elements per box: one 128-byte swizzle row
+constexpr int kKB = 1;         // boxes per stage (2 and 4 measured no faster on GB300)
+constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
 constexpr int kEpiThreads = 128;
+constexpr int kReduceUnroll = 8;  // independent partial-sum loads in flight per thread
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of GPU time per wait
 constexpr int kStatusTimeout = -5;                // MHC_ERR_TIMEOUT
 
 __device__ int g_device_status;
 
-template <int NPAD>
+// NPAD: MMA N (N padded to 16); KB: 64-column boxes per stage; CPS: CTAs
+// meant to share one SM (shared memory split between them; 1 is used, 2
+// measured slower).
+template <int NPAD, int KB, int CPS>
 struct Cfg {
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = NPAD * kBK * 2;
-    static constexpr int kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = (200 * 1024) / kStageBytes;
+    static constexpr int kBoxA = kBM * kBK * 2;    // one 128 × 64 bf16 box of X
+    static constexpr int kBoxB = NPAD * kBK * 2;   // one NPAD × 64 bf16 box of φᵀ
+    static constexpr int kABytes = KB * kBoxA;     // A boxes of a stage, then its B boxes
+    static constexpr int kStageBytes = KB * (kBoxA + kBoxB);
+    static constexpr int kStages = (CPS == 1 ? 200 * 1024 : 100 * 1024) / kStageBytes;
     static constexpr int kTmemCols =
         2 * NPAD <= 32 ? 32 : (2 * NPAD <= 64 ? 64 : (2 * NPAD <= 128 ? 128 : 256));
-    static constexpr int kBarrierBytes = 256;
-    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarrierBytes;
+    static constexpr int kBarrierBytes = 512;
+    static constexpr int kSsBytes = 2 * kBM * 4;  // square-sum hand-over, double-buffered
+    static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kSsBytes + kBarrierBytes;
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "MMA N for M=128");
     static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
-    static_assert(kStages >= 4, "pipeline depth");
+    static_assert(kStages >= 2, "pipeline depth");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-    static_assert((2 * kStages + 6) * 8 + 16 <= kBarrierBytes, "barrier area");
+    static_assert((2 * kStages + 10) * 8 + 16 <= kBarrierBytes, "barrier area");
 };
 
 // Static stream-K schedule: CTA c owns units [lo(c), lo(c+1)).
@@ -106,21 +116,24 @@ __device__ __forceinline__ void raise_timeout(volatile int *abort_flag) {
     atomicExch(&g_device_status, kStatusTimeout);
 }
 
-template <int NPAD>
+template <int NPAD, int KB, int CPS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
                 int *__restrict__ tile_tickets, float *__restrict__ partials)
 {
-    using C = Cfg<NPAD>;
+    using C = Cfg<NPAD, KB, CPS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes);
+    float *ss_buf = reinterpret_cast<float *>(smem + C::kStages * C::kStageBytes);  // [2][128]
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kStages * C::kStageBytes + C::kSsBytes);
     uint64_t *empty = full + C::kStages;
-    uint64_t *acc_full = empty + C::kStages;  // [2]
-    uint64_t *acc_empty = acc_full + 2;       // [2]
-    uint64_t *epi_bar = acc_empty + 2;        // epilogue group barrier
+    uint64_t *acc_full = empty + C::kStages;  // [2] MMA -> epilogue
+    uint64_t *acc_empty = acc_full + 2;       // [2] epilogue -> MMA
+    uint64_t *ss_full = acc_empty + 2;        // [2] square-sum -> epilogue
+    uint64_t *ss_empty = ss_full + 2;         // [2] epilogue -> square-sum
+    uint64_t *epi_bar = ss_empty + 2;         // epilogue group barrier
     uint64_t *drain_bar = epi_bar + 1;        // MMA drain after an abort
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(drain_bar + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
@@ -138,6 +151,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         for (int a = 0; a < 2; ++a) {
             ptx::mbar_init(&acc_full[a], 1);
             ptx::mbar_init(&acc_empty[a], 4);
+            ptx::mbar_init(&ss_full[a], 4);
+            ptx::mbar_init(&ss_empty[a], 4);
         }
         ptx::mbar_init(epi_bar, kEpiThreads);
         ptx::mbar_init(drain_bar, 1);
@@ -178,8 +193,14 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     uint8_t *a = smem + stage * C::kStageBytes;
                     ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
-                    ptx::tma_load_2d(a, &tm_x, kb * kBK, sg.m * kBM, &full[stage], pol_x);
-                    ptx::tma_load_2d(a + C::kABytes, &tm_w, kb * kBK, 0, &full[stage], pol_w);
+#pragma unroll
+                    for (int b = 0; b < KB; ++b)  // boxes past K read as zeros
+                        ptx::tma_load_2d(a + b * C::kBoxA, &tm_x, (kb * KB + b) * kBK, sg.m * kBM,
+                                         &full[stage], pol_x);
+#pragma unroll
+                    for (int b = 0; b < KB; ++b)
+                        ptx::tma_load_2d(a + C::kABytes + b * C::kBoxB, &tm_w, (kb * KB + b) * kBK,
+                                         0, &full[stage], pol_w);
                     ++issued;
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
@@ -224,13 +245,17 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     ptx::tc_fence_after();
                     const uint32_t a_addr = ptx::smem_u32(smem + stage * C::kStageBytes);
-                    const uint64_t a_desc = ptx::smem_desc_sw128(a_addr);
-                    const uint64_t b_desc = ptx::smem_desc_sw128(a_addr + C::kABytes);
 #pragma unroll
-                    for (int kk = 0; kk < kBK / 16; ++kk) {
-                        // advancing K by 16 bf16 = 32 bytes inside the swizzle row
-                        ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
-                                      (kb > sg.k0 || kk > 0) ? 1u : 0u);
+                    for (int b = 0; b < KB; ++b) {
+                        const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + b * C::kBoxA);
+                        const uint64_t b_desc =
+                            ptx::smem_desc_sw128(a_addr + C::kABytes + b * C::kBoxB);
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            // advancing K by 16 bf16 = 32 bytes inside the swizzle row
+                            ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
+                                          (kb > sg.k0 || b > 0 || kk > 0) ? 1u : 0u);
+                        }
                     }
                     ptx::mma_commit(&empty[stage]);  // frees the stage once these MMAs finish
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
@@ -247,13 +272,11 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 ptx::mbar_wait_bounded(drain_bar, 0, &never, kWaitLimitNs);
             }
         }
-    } else {
-        // ------------------------------- square-sum + epilogue (warps 2..5)
-        const int q = warp & 3;  // TMEM lane quarter this warp may access
-        const int row = q * 32 + lane;
-        const int et = threadIdx.x - 64;  // 0..127 within the epilogue group
+    } else if (warp < 6) {
+        // ---------------------------------------- square-sum (warps 2..5)
+        const int row = (warp - 2) * 32 + lane;
         int stage = 0;
-        uint32_t phase = 0, epi_phase = 0;
+        uint32_t phase = 0;
         int seg = 0;
         SegIter it{u_begin, u_end, sch.kbt};
         Segment sg;
@@ -268,10 +291,11 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 }
                 const uint8_t *arow = smem + stage * C::kStageBytes + row * 128;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // 16-byte chunk j of the row lives at chunk (j ^ row%8) (128-byte
-                    // swizzle); a row sum needs every chunk once, in any order.
-                    const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+                for (int j = 0; j < 8 * KB; ++j) {
+                    // 16-byte chunk j%8 of the row in box j/8 lives at chunk (j ^ row%8)
+                    // (128-byte swizzle); a row sum needs every chunk once, in any order.
+                    const uint4 v = *reinterpret_cast<const uint4 *>(
+                        arow + (j >> 3) * C::kBoxA + (((j & 7) ^ (row & 7)) << 4));
                     float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y), a3 = bf16_hi(v.y);
                     float a4 = bf16_lo(v.z), a5 = bf16_hi(v.z), a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
                     ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
@@ -284,10 +308,32 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (++stage == C::kStages) { stage = 0; phase ^= 1; }
             }
             if (!ok) break;
-
-            // accumulator of this segment -> registers
+            // hand the segment's row sums to the epilogue warps
+            const int buf = seg & 1;
+            if (!ptx::mbar_wait_bounded(&ss_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag,
+                                        kWaitLimitNs)) {
+                raise_timeout(abort_flag);
+                break;
+            }
+            ss_buf[buf * kBM + row] = (ss0 + ss1) + (ss2 + ss3);
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ss_full[buf]);
+            ++seg;
+        }
+    } else {
+        // ----------------------------------------------- epilogue (warps 6..9)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 192;  // 0..127 within the epilogue group
+        uint32_t epi_phase = 0;
+        int seg = 0;
+        SegIter it{u_begin, u_end, sch.kbt};
+        Segment sg;
+        while (it.next(sg)) {
+            // accumulator and square-sum of this segment -> registers
             const int acc = seg & 1;
-            if (!ptx::mbar_wait_bounded(&acc_full[acc], (seg >> 1) & 1, abort_flag, kWaitLimitNs)) {
+            const uint32_t par = (seg >> 1) & 1;
+            if (!ptx::mbar_wait_bounded(&acc_full[acc], par, abort_flag, kWaitLimitNs)) {
                 raise_timeout(abort_flag);
                 break;
             }
@@ -306,9 +352,15 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+            if (!ptx::mbar_wait_bounded(&ss_full[acc], par, abort_flag, kWaitLimitNs)) {
+                raise_timeout(abort_flag);
+                break;
+            }
+            const float ss = ss_buf[acc * kBM + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ss_empty[acc]);
             ++seg;
 
-            const float ss = (ss0 + ss1) + (ss2 + ss3);
             const int64_t row0 = static_cast<int64_t>(sg.m) * kBM;
             const int64_t grow = row0 + row;
             if (sg.k0 == 0 && sg.k1 == sch.kbt) {
@@ -342,19 +394,35 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
             if (*is_last) {
                 __threadfence();
-                // fixed-order sum over the contributors first..last
+                // fixed-order sum over the contributors first..last, kReduceUnroll
+                // independent items per thread at a time
                 const int64_t rows = (B - row0) < kBM ? (B - row0) : kBM;
                 const int items = static_cast<int>(rows) * stride;
-                const int64_t slot0 = static_cast<int64_t>(first + sg.m);
-                for (int i = et; i < items; i += kEpiThreads) {
-                    float s = 0.f;
-                    for (int c = 0; c <= last - first; ++c)
-                        s += __ldcg(partials + (slot0 + c) * kBM * stride + i);
-                    const int rr = i / stride, cc = i - rr * stride;
-                    if (cc < N)
-                        Y[(row0 + rr) * N + cc] = s;
-                    else
-                        r[row0 + rr] = sqrtf(s / static_cast<float>(K));
+                const float *p0 = partials + static_cast<int64_t>(first + sg.m) * kBM * stride;
+                const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
+                const int nc = last - first + 1;
+                for (int i0 = et; i0 < items; i0 += kEpiThreads * kReduceUnroll) {
+                    float acc_s[kReduceUnroll];
+#pragma unroll
+                    for (int u = 0; u < kReduceUnroll; ++u) acc_s[u] = 0.f;
+                    for (int c = 0; c < nc; ++c) {
+                        const float *pc = p0 + c * slot_stride;
+#pragma unroll
+                        for (int u = 0; u < kReduceUnroll; ++u) {
+                            const int i = i0 + u * kEpiThreads;
+                            if (i < items) acc_s[u] += __ldcg(pc + i);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kReduceUnroll; ++u) {
+                        const int i = i0 + u * kEpiThreads;
+                        if (i >= items) break;
+                        const int rr = i / stride, cc = i - rr * stride;
+                        if (cc < N)
+                            Y[(row0 + rr) * N + cc] = acc_s[u];
+                        else
+                            r[row0 + rr] = sqrtf(acc_s[u] / static_cast<float>(K));
+                    }
                 }
                 if (et == 0) tile_tickets[sg.m] = 0;
             }
@@ -365,7 +433,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     __syncthreads();
     if (warp == 1) {
         ptx::tc_fence_after();
-        ptx::tmem_dealloc<Cfg<NPAD>::kTmemCols>(tmem_base);
+        ptx::tmem_dealloc<C::kTmemCols>(tmem_base);
     }
 }
 
@@ -412,13 +480,13 @@ int npad_of(int n)
 }
 
 // Grid: one CTA per SM, but no more than 32 contributors per token tile (the
-// last arriver's fixed-order sum grows with the fan-in) and at least one K
-// block per CTA.
+// last arriver's fixed-order sum grows with the fan-in) and at least one
+// stage of K per CTA.
 Sched make_sched(int64_t B, int n, int64_t C, int num_sms)
 {
     Sched s;
     s.m_tiles = static_cast<int>((B + kBM - 1) / kBM);
-    s.kbt = static_cast<int>((n * C + kBK - 1) / kBK);
+    s.kbt = static_cast<int>((n * C + kBK * kKB - 1) / (kBK * kKB));
     s.total = static_cast<int64_t>(s.m_tiles) * s.kbt;
     int64_t g = num_sms;
     if (g > 32LL * s.m_tiles) g = 32LL * s.m_tiles;
@@ -430,25 +498,47 @@ Sched make_sched(int64_t B, int n, int64_t C, int num_sms)
 
 size_t tickets_bytes(int m_tiles) { return (static_cast<size_t>(m_tiles) * 4 + 255) / 256 * 256; }
 
-template <int NPAD>
-cudaError_t launch_npad(const CUtensorMap &tx, const CUtensorMap &tw, int64_t B, int N, int K,
-                        const Sched &s, float *Y, float *r, int *tickets, float *partials,
-                        cudaStream_t stream, int device)
+struct LaunchArgs {
+    const CUtensorMap *tx, *tw;
+    int64_t B;
+    int N, K;
+    Sched s;
+    float *Y, *r;
+    int *tickets;
+    float *partials;
+    cudaStream_t stream;
+    int device;
+};
+
+template <int NPAD, int KB, int CPS>
+cudaError_t launch_cfg(const LaunchArgs &a)
 {
-    using Cf = Cfg<NPAD>;
+    using Cf = Cfg<NPAD, KB, CPS>;
     static uint64_t configured = 0;  // one bit per device
     static std::mutex mu;
-    if (device < 64 && !((configured >> device) & 1)) {
+    if (a.device < 64 && !((configured >> a.device) & 1)) {
         std::lock_guard<std::mutex> lock(mu);
-        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD, KB, CPS>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
-        configured |= 1ull << device;
+        configured |= 1ull << a.device;
     }
-    gemm_rms_kernel<NPAD><<<s.grid, kThreads, Cf::kSmemBytes, stream>>>(tx, tw, B, N, K, s, Y, r,
-                                                                       tickets, partials);
+    gemm_rms_kernel<NPAD, KB, CPS><<<a.s.grid, kThreads, Cf::kSmemBytes, a.stream>>>(
+        *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r, a.tickets, a.partials);
     return cudaGetLastError();
+}
+
+cudaError_t dispatch(int npad, const LaunchArgs &a)
+{
+    switch (npad) {
+    case 16: return launch_cfg<16, kKB, 1>(a);
+    case 32: return launch_cfg<32, kKB, 1>(a);
+    case 48: return launch_cfg<48, kKB, 1>(a);
+    case 64: return launch_cfg<64, kKB, 1>(a);
+    case 80: return launch_cfg<80, kKB, 1>(a);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -482,15 +572,9 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
     if (e != cudaSuccess) return e;
     int device = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
-    const int Ki = static_cast<int>(K);
-    switch (npad) {
-    case 16: return launch_npad<16>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
-    case 32: return launch_npad<32>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
-    case 48: return launch_npad<48>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
-    case 64: return launch_npad<64>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
-    case 80: return launch_npad<80>(tx, tw, B, N, Ki, s, Y, r, tickets, partials, stream, device);
-    default: return cudaErrorInvalidValue;
-    }
+    const LaunchArgs a{&tx, &tw, B, N, static_cast<int>(K), s, Y, r, tickets, partials, stream,
+                       device};
+    return dispatch(npad, a);
 }
 
 cudaError_t read_and_clear_device_status(int *status)

@@ -105,7 +105,7 @@ int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int
  *   H_res     = Sinkhorn–Knopp: start from exp(H̃_res) as an n×n matrix, then
  *               `iters` times divide each row by its sum, then each column
  *               by its sum.  iters = 0 returns exp(H̃_res) unnormalised.
- * The n×n iteration runs in registers, one token per thread.
+ * The n×n iteration runs in registers: n lanes of a warp per token, one row per lane.
  */
 int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post,
                float alpha_res, const float *bias, int iters, int64_t B, int n,
