@@ -245,6 +245,45 @@ def tokens_per_second(tokens_per_rank: int, world: int, steps: int, ms_total: fl
 # ------------------------------------------------------------------ GPU arm
 
 
+def forward_latency(mhc, step, stream, barrier, steps, warmup) -> dict:
+    """Microseconds per mhc_forward: back-to-back stream launches (includes the
+    host's call overhead when it exceeds the GPU time) and replays of a CUDA
+    graph holding `steps` forwards (GPU time only)."""
+    import torch
+
+    for _ in range(max(warmup, 3)):
+        step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    barrier()
+    us_stream = 1e3 * e0.elapsed_time(e1) / steps
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(steps):
+                step_on = torch.cuda.current_stream()
+                step(step_on)
+    stream.wait_stream(side)
+    for _ in range(2):
+        g.replay()
+    barrier()
+    reps = 5
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    barrier()
+    us_graph = 1e3 * e0.elapsed_time(e1) / (reps * steps)
+    return {"us_per_forward_stream": us_stream, "us_per_forward_graph": us_graph,
+            "forwards_timed": steps}
+
+
 def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out) -> dict:
     """Mean CUDA-event time (ms) of each kernel over `steps` passes of the four
     entry points, events recorded between launches on the launching stream."""
@@ -286,8 +325,9 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of identical load kept up for the clock samples")
-    ap.add_argument("--mode", default="full", choices=["full", "kernels"],
-                    help="kernels: only the per-kernel loop (small runs for ncu captures)")
+    ap.add_argument("--mode", default="full", choices=["full", "kernels", "latency"],
+                    help="kernels: only the per-kernel loop (small runs for ncu captures); "
+                         "latency: microseconds per mhc_forward (stream and CUDA graph)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -328,10 +368,11 @@ def main() -> int:
     out = mhc.alloc_outputs(B, n, C, dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def step(on_stream=None):
         mhc.mhc_forward(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
                         wl.iters, B, n, C, out["Y"], out["r"], out["H_pre"], out["H_post"],
-                        out["H_res"], out["F_pre"], out["X_next"], out["ws"], stream)
+                        out["H_res"], out["F_pre"], out["X_next"], out["ws"],
+                        on_stream if on_stream is not None else stream)
 
     def barrier():
         if dist is not None:
@@ -344,6 +385,14 @@ def main() -> int:
         gpu_id = str(local)
     sampler = ClockSampler(gpu_id)
     time.sleep(0.3)
+
+    if args.mode == "latency":
+        sampler.stop()
+        res = forward_latency(mhc, step, stream, barrier, args.steps, args.warmup)
+        if rank == 0:
+            print(json.dumps({"mode": "latency", "workload": wl.name, "B": B, "n": n, "C": C,
+                              **res}), flush=True)
+        return 0
 
     if args.mode == "kernels":
         for _ in range(args.warmup):

@@ -45,6 +45,8 @@ __global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__
 {
     const int64_t C8 = C >> 3;
     const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    ptx::pdl_wait();  // H_pre comes from the previous kernel
+    ptx::pdl_trigger();
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
         float h[n];
 #pragma unroll
@@ -78,6 +80,8 @@ __global__ void post_res_apply_kernel(const uint16_t *X, const uint16_t *__restr
     __shared__ float hs[n * n + n];
     const int64_t C8 = C >> 3;
     const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    ptx::pdl_wait();  // H_res and H_post come from earlier kernels
+    ptx::pdl_trigger();
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
         __syncthreads();  // previous token's coefficients are no longer read
         for (int t = threadIdx.x; t < n * n + n; t += blockDim.x)
@@ -139,7 +143,7 @@ cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, i
     const dim3 grid = apply_grid(B, C8, threads);
     switch (n) {
 #define MHC_CASE(k) \
-    case k: pre_apply_kernel<k><<<grid, threads, 0, stream>>>(X, H_pre, B, C, F_pre); break;
+    case k: return launch_pdl(pre_apply_kernel<k>, grid, dim3(threads), 0, stream, X, H_pre, B, C, F_pre);
         MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
         MHC_CASE(8)
 #undef MHC_CASE
@@ -156,11 +160,10 @@ cudaError_t launch_post_res_apply(const uint16_t *X, const uint16_t *F_out, cons
     const int threads = block_threads(C8);
     const dim3 grid = apply_grid(B, C8, threads);
     switch (n) {
-#define MHC_CASE(k)                                                                         \
-    case k:                                                                                 \
-        post_res_apply_kernel<k><<<grid, threads, 0, stream>>>(X, F_out, H_res, H_post, B, C, \
-                                                                 X_next);                   \
-        break;
+#define MHC_CASE(k)                                                                       \
+    case k:                                                                               \
+        return launch_pdl(post_res_apply_kernel<k>, grid, dim3(threads), 0, stream, X, F_out, \
+                          H_res, H_post, B, C, X_next);
         MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
         MHC_CASE(8)
 #undef MHC_CASE

@@ -24,6 +24,7 @@
 #include <cstdint>
 
 #include "mhc_internal.h"
+#include "ptx.cuh"
 
 namespace mhc {
 namespace {
@@ -64,6 +65,8 @@ coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_
     // (32 mod n of them) sit out
     const unsigned mask = kGroups * n == 32 ? 0xFFFFFFFFu : ((1u << (kGroups * n)) - 1u);
     if (g >= kGroups) return;
+    ptx::pdl_wait();  // Y and r come from the previous kernel
+    ptx::pdl_trigger();
 
     const int64_t t = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kGroups + g;
     const bool valid = t < B;
@@ -119,9 +122,8 @@ cudaError_t launch_n(const float *Y, const float *r, float a_pre, float a_post, 
 {
     constexpr int64_t tokens_per_block = (kThreads / 32) * (32 / n);
     const int64_t blocks = (B + tokens_per_block - 1) / tokens_per_block;
-    coeffs_kernel<n><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(
-        Y, r, a_pre, a_post, a_res, bias, iters, B, H_pre, H_post, H_res);
-    return cudaGetLastError();
+    return launch_pdl(coeffs_kernel<n>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
+                      stream, Y, r, a_pre, a_post, a_res, bias, iters, B, H_pre, H_post, H_res);
 }
 
 }  // namespace

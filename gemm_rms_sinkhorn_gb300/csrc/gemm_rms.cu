@@ -42,7 +42,8 @@ constexpr int kBK = 64;        // K elements per box: one 128-byte swizzle row
 constexpr int kKB = 1;         // boxes per stage (2 and 4 measured no faster on GB300)
 constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
 constexpr int kEpiThreads = 128;
-constexpr int kReduceUnroll = 8;  // independent partial-sum loads in flight per thread
+constexpr int kReduceItems = 4;   // outputs per thread per round of the fixed-order sum
+constexpr int kReduceBatch = 8;   // contributors loaded per batch: 32 loads in flight
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of GPU time per wait
 constexpr int kStatusTimeout = -5;                // MHC_ERR_TIMEOUT
 
@@ -169,6 +170,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // everything above is on-chip set-up; global memory is touched only after
+    // the previous kernel in the stream has completed
+    ptx::pdl_wait();
 
     const int64_t u_begin = sch.lo(cta), u_end = sch.lo(cta + 1);
 
@@ -394,27 +398,35 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
             if (*is_last) {
                 __threadfence();
-                // fixed-order sum over the contributors first..last, kReduceUnroll
-                // independent items per thread at a time
+                // fixed-order sum over the contributors first..last: a batch of
+                // contributors x items is loaded before it is added, in order
                 const int64_t rows = (B - row0) < kBM ? (B - row0) : kBM;
                 const int items = static_cast<int>(rows) * stride;
                 const float *p0 = partials + static_cast<int64_t>(first + sg.m) * kBM * stride;
                 const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
                 const int nc = last - first + 1;
-                for (int i0 = et; i0 < items; i0 += kEpiThreads * kReduceUnroll) {
-                    float acc_s[kReduceUnroll];
+                for (int i0 = et; i0 < items; i0 += kEpiThreads * kReduceItems) {
+                    float acc_s[kReduceItems];
 #pragma unroll
-                    for (int u = 0; u < kReduceUnroll; ++u) acc_s[u] = 0.f;
-                    for (int c = 0; c < nc; ++c) {
-                        const float *pc = p0 + c * slot_stride;
+                    for (int u = 0; u < kReduceItems; ++u) acc_s[u] = 0.f;
+                    for (int c0 = 0; c0 < nc; c0 += kReduceBatch) {
+                        float vb[kReduceBatch][kReduceItems];
 #pragma unroll
-                        for (int u = 0; u < kReduceUnroll; ++u) {
-                            const int i = i0 + u * kEpiThreads;
-                            if (i < items) acc_s[u] += __ldcg(pc + i);
-                        }
+                        for (int c = 0; c < kReduceBatch; ++c)
+#pragma unroll
+                            for (int u = 0; u < kReduceItems; ++u) {
+                                const int i = i0 + u * kEpiThreads;
+                                vb[c][u] = (c0 + c < nc && i < items)
+                                               ? __ldcg(p0 + (c0 + c) * slot_stride + i)
+                                               : 0.f;  // acc + 0 is exact: acc is never -0
+                            }
+#pragma unroll
+                        for (int c = 0; c < kReduceBatch; ++c)
+#pragma unroll
+                            for (int u = 0; u < kReduceItems; ++u) acc_s[u] += vb[c][u];
                     }
 #pragma unroll
-                    for (int u = 0; u < kReduceUnroll; ++u) {
+                    for (int u = 0; u < kReduceItems; ++u) {
                         const int i = i0 + u * kEpiThreads;
                         if (i >= items) break;
                         const int rr = i / stride, cc = i - rr * stride;
@@ -431,10 +443,24 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 
     ptx::tc_fence_before();
     __syncthreads();
+    // Let the next kernel launch only now: CTAs of a dependent kernel that sit
+    // resident in pdl_wait next to this one for its whole run slow it down
+    // (measured: +13% at B=16384), while a trigger at the end still hides
+    // the launch latency.
+    ptx::pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc<C::kTmemCols>(tmem_base);
     }
+}
+
+// Clears the tile tickets of a call before its GEMM kernel runs.
+__global__ void zero_tickets_kernel(int *tickets, int count)
+{
+    ptx::pdl_wait();
+    ptx::pdl_trigger();
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x)
+        tickets[i] = 0;
 }
 
 // ------------------------------------------------------------------ host
@@ -524,9 +550,9 @@ cudaError_t launch_cfg(const LaunchArgs &a)
         if (e != cudaSuccess) return e;
         configured |= 1ull << a.device;
     }
-    gemm_rms_kernel<NPAD, KB, CPS><<<a.s.grid, kThreads, Cf::kSmemBytes, a.stream>>>(
-        *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r, a.tickets, a.partials);
-    return cudaGetLastError();
+    return launch_pdl(gemm_rms_kernel<NPAD, KB, CPS>, dim3(a.s.grid), dim3(kThreads),
+                      Cf::kSmemBytes, a.stream, *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r,
+                      a.tickets, a.partials);
 }
 
 cudaError_t dispatch(int npad, const LaunchArgs &a)
@@ -568,7 +594,9 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
     int *tickets = static_cast<int *>(workspace);
     float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
                                                 tickets_bytes(s.m_tiles));
-    cudaError_t e = cudaMemsetAsync(tickets, 0, static_cast<size_t>(s.m_tiles) * 4, stream);
+    const int zero_blocks = s.m_tiles < 256 * 64 ? (s.m_tiles + 255) / 256 : 64;
+    cudaError_t e = launch_pdl(zero_tickets_kernel, dim3(zero_blocks), dim3(256), 0, stream,
+                               tickets, s.m_tiles);
     if (e != cudaSuccess) return e;
     int device = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;

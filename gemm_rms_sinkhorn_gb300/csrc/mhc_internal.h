@@ -9,6 +9,28 @@
 
 namespace mhc {
 
+// Launches `kernel` with programmatic stream serialisation: its CTAs may
+// start while the previous kernel in the stream finishes, and every kernel
+// of this library calls pdl_wait() before it touches global memory, so the
+// launch latency and prologue overlap the predecessor without changing the
+// stream order of memory accesses.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // N = n² + 2n coefficient columns per token.
 inline int num_coeffs(int n) { return n * n + 2 * n; }
 

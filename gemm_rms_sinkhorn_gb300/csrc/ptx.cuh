@@ -203,6 +203,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------ programmatic dependent launch
+
+// Blocks until the grids this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) have
+// completed and their memory is visible.  A no-op otherwise.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream start launching its CTAs (they wait in
+// pdl_wait until this grid completes).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------ streaming access
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
