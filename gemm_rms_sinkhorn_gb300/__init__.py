@@ -47,6 +47,9 @@ _SIGS = {
                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
     "mhc_gemm_rms_noalloc": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp], _i32),
+    # test hook (include/mhc_testing.h), not part of the stable API
+    "mhc_testing_gemm_rms_stalled": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _i64,
+                                      ctypes.c_uint64, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)

@@ -9,6 +9,7 @@
 
 #include "mhc.h"
 #include "mhc_internal.h"
+#include "mhc_testing.h"
 
 namespace mhc {
 
@@ -125,6 +126,31 @@ size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 
 using namespace mhc;
 
+static int gemm_rms_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C,
+                            float *Y, float *r, void *workspace, size_t workspace_bytes,
+                            mhc_stream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 2));
+    MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[2].bytes = need;
+    MHC_TRY(check_ptrs(outs + 2, 1));
+    MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    return cuda_status(launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
+                                       reinterpret_cast<cudaStream_t>(stream), wait_limit_ns,
+                                       stall_stage));
+}
+
 extern "C" {
 
 const char *mhc_status_str(int status)
@@ -152,24 +178,20 @@ size_t mhc_workspace_bytes(int64_t B, int n, int64_t C)
 int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C, float *Y,
                  float *r, void *workspace, size_t workspace_bytes, mhc_stream_t stream)
 {
-    MHC_TRY(check_shape(B, n, C, true));
-    if (B == 0) return MHC_OK;
-    const int N = num_coeffs(n);
-    const int64_t K = n * C;
-    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)}};
-    Buf outs[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {workspace, workspace_bytes}};
-    MHC_TRY(check_ptrs(ins, 2));
-    MHC_TRY(check_ptrs(outs, 2));
-    MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
-    DeviceInfo info;
-    MHC_TRY(check_device(&info));
-    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
-    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
-    outs[2].bytes = need;
-    MHC_TRY(check_ptrs(outs + 2, 1));
-    MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
-    return cuda_status(launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
-                                       reinterpret_cast<cudaStream_t>(stream)));
+    return gemm_rms_checked(X, phi_t, B, n, C, Y, r, workspace, workspace_bytes, stream,
+                            kWaitLimitNs, -1);
+}
+
+int mhc_testing_gemm_rms_stalled(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n,
+                                 int64_t C, float *Y, float *r, void *workspace,
+                                 size_t workspace_bytes, int64_t stall_stage,
+                                 uint64_t wait_limit_ns, mhc_stream_t stream)
+{
+    const uint64_t lo = 1000000ull;
+    const uint64_t limit = wait_limit_ns < lo ? lo : (wait_limit_ns > kWaitLimitNs ? kWaitLimitNs
+                                                                                   : wait_limit_ns);
+    return gemm_rms_checked(X, phi_t, B, n, C, Y, r, workspace, workspace_bytes, stream, limit,
+                            stall_stage);
 }
 
 int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post, float alpha_res,

@@ -44,7 +44,6 @@ constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epil
 constexpr int kEpiThreads = 128;
 constexpr int kReduceItems = 4;   // outputs per thread per round of the fixed-order sum
 constexpr int kReduceBatch = 8;   // contributors loaded per batch: 32 loads in flight
-constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s of GPU time per wait
 constexpr int kStatusTimeout = -5;                // MHC_ERR_TIMEOUT
 
 __device__ int g_device_status;
@@ -66,7 +65,7 @@ struct Cfg {
     static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kSsBytes + kBarrierBytes;
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "MMA N for M=128");
     static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
-    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kStages >= 2 && kStages <= 32, "pipeline depth (one bit per stage)");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert((2 * kStages + 10) * 8 + 16 <= kBarrierBytes, "barrier area");
 };
@@ -105,9 +104,10 @@ struct SegIter {
 
 // Group barrier of the 128 epilogue threads on an mbarrier, so that the wait
 // is bounded like every other wait in the kernel.
-__device__ __forceinline__ bool epi_sync(uint64_t *bar, uint32_t &phase, volatile int *abort_flag) {
+__device__ __forceinline__ bool epi_sync(uint64_t *bar, uint32_t &phase, volatile int *abort_flag,
+                                         uint64_t limit_ns) {
     ptx::mbar_arrive(bar);
-    const bool ok = ptx::mbar_wait_bounded(bar, phase, abort_flag, kWaitLimitNs);
+    const bool ok = ptx::mbar_wait_bounded(bar, phase, abort_flag, limit_ns);
     phase ^= 1;
     return ok;
 }
@@ -121,7 +121,8 @@ template <int NPAD, int KB, int CPS>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
-                int *__restrict__ tile_tickets, float *__restrict__ partials)
+                int *__restrict__ tile_tickets, float *__restrict__ partials,
+                uint64_t wait_limit_ns, int64_t stall_stage)
 {
     using C = Cfg<NPAD, KB, CPS>;
     extern __shared__ uint8_t smem_raw[];
@@ -183,42 +184,47 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const uint64_t pol_w = ptx::policy_evict_last();   // φ is re-read by every CTA
             int stage = 0;
             uint32_t phase = 0;
-            int64_t issued = 0;
+            uint32_t issued_mask = 0, issued_parity = 0;  // stages with a TMA issued, its phase
+            int64_t count = 0;
             SegIter it{u_begin, u_end, sch.kbt};
             Segment sg;
             bool ok = true;
             while (ok && it.next(sg)) {
-                for (int kb = sg.k0; kb < sg.k1; ++kb) {
+                for (int kb = sg.k0; kb < sg.k1; ++kb, ++count) {
                     if (!ptx::mbar_wait_bounded(&empty[stage], phase ^ 1, abort_flag,
-                                                kWaitLimitNs)) {
+                                                wait_limit_ns)) {
                         raise_timeout(abort_flag);
                         ok = false;
                         break;
                     }
-                    uint8_t *a = smem + stage * C::kStageBytes;
-                    ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+                    // test hook: CTA 0 leaves one stage unfilled, so its consumers'
+                    // bounded waits run out (stall_stage < 0 in normal calls)
+                    if (!(cta == 0 && count == stall_stage)) {
+                        uint8_t *a = smem + stage * C::kStageBytes;
+                        ptx::mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
 #pragma unroll
-                    for (int b = 0; b < KB; ++b)  // boxes past K read as zeros
-                        ptx::tma_load_2d(a + b * C::kBoxA, &tm_x, (kb * KB + b) * kBK, sg.m * kBM,
-                                         &full[stage], pol_x);
+                        for (int b = 0; b < KB; ++b)  // boxes past K read as zeros
+                            ptx::tma_load_2d(a + b * C::kBoxA, &tm_x, (kb * KB + b) * kBK,
+                                             sg.m * kBM, &full[stage], pol_x);
 #pragma unroll
-                    for (int b = 0; b < KB; ++b)
-                        ptx::tma_load_2d(a + C::kABytes + b * C::kBoxB, &tm_w, (kb * KB + b) * kBK,
-                                         0, &full[stage], pol_w);
-                    ++issued;
+                        for (int b = 0; b < KB; ++b)
+                            ptx::tma_load_2d(a + C::kABytes + b * C::kBoxB, &tm_w,
+                                             (kb * KB + b) * kBK, 0, &full[stage], pol_w);
+                        issued_mask |= 1u << stage;
+                        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+                    }
                     if (++stage == C::kStages) { stage = 0; phase ^= 1; }
                 }
             }
             if (!ok) {
                 // Let the copies already issued land before shared memory is released:
-                // the last min(issued, stages) stages each hold one outstanding phase.
-                int64_t pending = issued < C::kStages ? issued : C::kStages;
-                int s = stage;
-                uint32_t ph = phase;
-                for (int64_t i = 0; i < pending; ++i) {
-                    if (--s < 0) { s = C::kStages - 1; ph ^= 1; }
+                // wait for the phase of each stage's last issue (already complete for
+                // stages whose data was consumed).
+                for (int s2 = 0; s2 < C::kStages; ++s2) {
+                    if (!((issued_mask >> s2) & 1u)) continue;
                     volatile int never = 0;
-                    ptx::mbar_wait_bounded(&full[s], ph, &never, kWaitLimitNs);
+                    ptx::mbar_wait_bounded(&full[s2], (issued_parity >> s2) & 1u, &never,
+                                           wait_limit_ns);
                 }
             }
         }
@@ -235,14 +241,14 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             while (ok && it.next(sg)) {
                 const int acc = seg & 1;
                 if (!ptx::mbar_wait_bounded(&acc_empty[acc], ((seg >> 1) & 1) ^ 1, abort_flag,
-                                            kWaitLimitNs)) {
+                                            wait_limit_ns)) {
                     raise_timeout(abort_flag);
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * NPAD);
                 for (int kb = sg.k0; kb < sg.k1; ++kb) {
-                    if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                    if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, wait_limit_ns)) {
                         raise_timeout(abort_flag);
                         ok = false;
                         break;
@@ -273,7 +279,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!ok || *abort_flag) {
                 ptx::mma_commit(drain_bar);
                 volatile int never = 0;
-                ptx::mbar_wait_bounded(drain_bar, 0, &never, kWaitLimitNs);
+                ptx::mbar_wait_bounded(drain_bar, 0, &never, wait_limit_ns);
             }
         }
     } else if (warp < 6) {
@@ -288,7 +294,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         while (ok && it.next(sg)) {
             float ss0 = 0.f, ss1 = 0.f, ss2 = 0.f, ss3 = 0.f;
             for (int kb = sg.k0; kb < sg.k1; ++kb) {
-                if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, kWaitLimitNs)) {
+                if (!ptx::mbar_wait_bounded(&full[stage], phase, abort_flag, wait_limit_ns)) {
                     raise_timeout(abort_flag);
                     ok = false;
                     break;
@@ -315,7 +321,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // hand the segment's row sums to the epilogue warps
             const int buf = seg & 1;
             if (!ptx::mbar_wait_bounded(&ss_empty[buf], ((seg >> 1) & 1) ^ 1, abort_flag,
-                                        kWaitLimitNs)) {
+                                        wait_limit_ns)) {
                 raise_timeout(abort_flag);
                 break;
             }
@@ -337,7 +343,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             // accumulator and square-sum of this segment -> registers
             const int acc = seg & 1;
             const uint32_t par = (seg >> 1) & 1;
-            if (!ptx::mbar_wait_bounded(&acc_full[acc], par, abort_flag, kWaitLimitNs)) {
+            if (!ptx::mbar_wait_bounded(&acc_full[acc], par, abort_flag, wait_limit_ns)) {
                 raise_timeout(abort_flag);
                 break;
             }
@@ -356,7 +362,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
-            if (!ptx::mbar_wait_bounded(&ss_full[acc], par, abort_flag, kWaitLimitNs)) {
+            if (!ptx::mbar_wait_bounded(&ss_full[acc], par, abort_flag, wait_limit_ns)) {
                 raise_timeout(abort_flag);
                 break;
             }
@@ -388,14 +394,14 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 mine[row * stride + N] = ss;
             }
             __threadfence();
-            if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
+            if (!epi_sync(epi_bar, epi_phase, abort_flag, wait_limit_ns)) { raise_timeout(abort_flag); break; }
             const int first = sch.owner(static_cast<int64_t>(sg.m) * sch.kbt);
             const int last = sch.owner(static_cast<int64_t>(sg.m + 1) * sch.kbt - 1);
             if (et == 0) {
                 const int prev = atomicAdd(&tile_tickets[sg.m], 1);
                 *is_last = (prev == last - first);
             }
-            if (!epi_sync(epi_bar, epi_phase, abort_flag)) { raise_timeout(abort_flag); break; }
+            if (!epi_sync(epi_bar, epi_phase, abort_flag, wait_limit_ns)) { raise_timeout(abort_flag); break; }
             if (*is_last) {
                 __threadfence();
                 // fixed-order sum over the contributors first..last: a batch of
@@ -534,6 +540,8 @@ struct LaunchArgs {
     float *partials;
     cudaStream_t stream;
     int device;
+    uint64_t wait_limit_ns;
+    int64_t stall_stage;
 };
 
 template <int NPAD, int KB, int CPS>
@@ -552,7 +560,7 @@ cudaError_t launch_cfg(const LaunchArgs &a)
     }
     return launch_pdl(gemm_rms_kernel<NPAD, KB, CPS>, dim3(a.s.grid), dim3(kThreads),
                       Cf::kSmemBytes, a.stream, *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r,
-                      a.tickets, a.partials);
+                      a.tickets, a.partials, a.wait_limit_ns, a.stall_stage);
 }
 
 cudaError_t dispatch(int npad, const LaunchArgs &a)
@@ -580,7 +588,7 @@ size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
 
 cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
                             int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                            cudaStream_t stream)
+                            cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
 {
     const int N = num_coeffs(n);
     const int64_t K = n * C;
@@ -601,7 +609,7 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
     int device = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     const LaunchArgs a{&tx, &tw, B, N, static_cast<int>(K), s, Y, r, tickets, partials, stream,
-                       device};
+                       device, wait_limit_ns, stall_stage};
     return dispatch(npad, a);
 }
 

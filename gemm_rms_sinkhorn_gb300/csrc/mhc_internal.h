@@ -44,10 +44,14 @@ struct DeviceInfo {
 cudaError_t current_device_info(DeviceInfo *info);
 
 // ---- step 1: GEMM + RMS (gemm_rms.cu)
+// Every wait inside the GEMM kernel gives up after this much GPU time.
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
 size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+// stall_stage >= 0 is a test hook: CTA 0 leaves that pipeline stage unfilled.
 cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
                             int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                            cudaStream_t stream);
+                            cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
+                            int64_t stall_stage = -1);
 cudaError_t read_and_clear_device_status(int *status);
 
 // ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
