@@ -50,6 +50,8 @@ _SIGS = {
     # test hook (include/mhc_testing.h), not part of the stable API
     "mhc_testing_gemm_rms_stalled": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _i64,
                                       ctypes.c_uint64, _vp], _i32),
+    "mhc_testing_forward_fused": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -157,6 +159,19 @@ def mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, 
                             _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
                             _stream(stream)),
            "mhc_forward")
+
+
+def mhc_testing_forward_fused(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B,
+                              n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    """Test hook: mhc_forward through the one-kernel steps 1-4a path."""
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_testing_forward_fused(
+        _ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), _ptr(F_out, bf, "F_out"), alpha_pre,
+        alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n, C, _ptr(Y, f, "Y"),
+        _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"), _ptr(H_post, f, "H_post"),
+        _ptr(H_res, f, "H_res"), _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
+        _stream(stream)), "mhc_testing_forward_fused")
 
 
 def mhc_gemm_rms_noalloc(X, phi_t, B, n, C, Y, r, stream=None):

@@ -113,6 +113,14 @@ int check_device(DeviceInfo *info)
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
 
 size_t bf16_bytes(int64_t count) { return static_cast<size_t>(count) * 2; }
+
+// Workspace of either forward path (and of mhc_gemm_rms), whichever is larger.
+size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
+{
+    const size_t a = gemm_rms_workspace_bytes(B, n, C, num_sms);
+    const size_t b = fused_pre_workspace_bytes(B, n, C, num_sms);
+    return a > b ? a : b;
+}
 size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 
 #define MHC_TRY(expr)                   \
@@ -125,6 +133,52 @@ size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 }  // namespace mhc
 
 using namespace mhc;
+
+static int forward_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                           float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                           int iters, int64_t B, int n, int64_t C, float *Y, float *r,
+                           float *H_pre, float *H_post, float *H_res, mhc_bf16 *F_pre,
+                           mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,
+                           mhc_stream_t stream, bool use_fused)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)},
+                       {F_out, bf16_bytes(B * C)}, {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {F_pre, bf16_bytes(B * C)},
+                  {X_next, bf16_bytes(B * K)},   {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 7));
+    MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = forward_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[7].bytes = need;
+    MHC_TRY(check_ptrs(outs + 7, 1));
+    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (use_fused) {
+        if (!fused_pre_eligible(B, n, C, info.num_sms)) return MHC_ERR_UNSUPPORTED;
+        // steps 1-4a in one kernel that reads X from HBM once
+        e = launch_fused_pre(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y,
+                             r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s);
+    } else {
+        e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
+        if (e == cudaSuccess)
+            e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
+                              H_post, H_res, s);
+        if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    }
+    if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
+    return cuda_status(e);
+}
 
 static int gemm_rms_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C,
                             float *Y, float *r, void *workspace, size_t workspace_bytes,
@@ -172,7 +226,7 @@ size_t mhc_workspace_bytes(int64_t B, int n, int64_t C)
     if (check_shape(B, n, C, true) != MHC_OK) return 0;
     DeviceInfo info;
     if (current_device_info(&info) != cudaSuccess) return 0;
-    return gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    return forward_workspace_bytes(B, n, C, info.num_sms);
 }
 
 int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C, float *Y,
@@ -254,43 +308,30 @@ int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
                 mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,
                 mhc_stream_t stream)
 {
-    MHC_TRY(check_shape(B, n, C, true));
-    if (iters < 0) return MHC_ERR_INVALID;
-    if (B == 0) return MHC_OK;
-    const int N = num_coeffs(n);
-    const int64_t K = n * C;
-    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)},
-                       {F_out, bf16_bytes(B * C)}, {bias, f32_bytes(N)}};
-    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
-                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
-                  {H_res, f32_bytes(B * n * n)}, {F_pre, bf16_bytes(B * C)},
-                  {X_next, bf16_bytes(B * K)},   {workspace, workspace_bytes}};
-    MHC_TRY(check_ptrs(ins, 4));
-    MHC_TRY(check_ptrs(outs, 7));
-    MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
-    DeviceInfo info;
-    MHC_TRY(check_device(&info));
-    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
-    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
-    outs[7].bytes = need;
-    MHC_TRY(check_ptrs(outs + 7, 1));
-    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
-    if (e == cudaSuccess)
-        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre, H_post,
-                          H_res, s);
-    if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
-    if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
-    return cuda_status(e);
+    return forward_checked(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
+                           C, Y, r, H_pre, H_post, H_res, F_pre, X_next, workspace,
+                           workspace_bytes, stream, false);
+}
+
+int mhc_testing_forward_fused(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                              float alpha_pre, float alpha_post, float alpha_res,
+                              const float *bias, int iters, int64_t B, int n, int64_t C, float *Y,
+                              float *r, float *H_pre, float *H_post, float *H_res,
+                              mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
+                              size_t workspace_bytes, mhc_stream_t stream)
+{
+    return forward_checked(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
+                           C, Y, r, H_pre, H_post, H_res, F_pre, X_next, workspace,
+                           workspace_bytes, stream, true);
 }
 
 int mhc_device_status(int *status)
 {
     if (status == nullptr) return MHC_ERR_INVALID;
-    int v = 0;
+    int v = 0, w = 0;
     if (read_and_clear_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
-    *status = v;
+    if (read_and_clear_fused_status(&w) != cudaSuccess) return MHC_ERR_CUDA;
+    *status = v != MHC_OK ? v : w;
     return MHC_OK;
 }
 

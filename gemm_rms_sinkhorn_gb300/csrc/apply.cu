@@ -20,24 +20,13 @@
 #include <cstdint>
 
 #include "mhc_internal.h"
+#include "mix.cuh"
 #include "ptx.cuh"
 
 namespace mhc {
 namespace {
 
 constexpr int kMaxGridY = 65535;
-
-__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8])
-{
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&f)[8])
-{
-    return make_uint4(pack_bf16_rn(f[0], f[1]), pack_bf16_rn(f[2], f[3]),
-                      pack_bf16_rn(f[4], f[5]), pack_bf16_rn(f[6], f[7]));
-}
 
 template <int n>
 __global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__restrict__ H_pre,
@@ -56,17 +45,7 @@ __global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__
             uint4 xv[n];
 #pragma unroll
             for (int i = 0; i < n; ++i) xv[i] = ptx::ld_stream_v4(x + i * C);
-            float acc[8], t[8];
-            unpack8(xv[0], t);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) acc[e] = h[0] * t[e];
-#pragma unroll
-            for (int i = 1; i < n; ++i) {
-                unpack8(xv[i], t);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(h[i], t[e], acc[e]);
-            }
-            ptx::st_stream_v4(F_pre + b * C + c8 * 8, pack8(acc));
+            ptx::st_stream_v4(F_pre + b * C + c8 * 8, pre_mix8<n>(h, xv));
         }
     }
 }

@@ -24,29 +24,13 @@
 #include <cstdint>
 
 #include "mhc_internal.h"
+#include "mix.cuh"
 #include "ptx.cuh"
 
 namespace mhc {
 namespace {
 
 constexpr int kThreads = 128;
-
-// Sum over the n lanes of a token group of v, identical on every lane.
-template <int n>
-__device__ __forceinline__ float group_sum(float v, int base, unsigned mask)
-{
-    if constexpr ((n & (n - 1)) == 0) {
-        // butterfly: a + b == b + a exactly, so every lane ends with the same value
-#pragma unroll
-        for (int off = 1; off < n; off <<= 1) v += __shfl_xor_sync(mask, v, off);
-        return v;
-    } else {
-        float s = __shfl_sync(mask, v, base);
-#pragma unroll
-        for (int k = 1; k < n; ++k) s += __shfl_sync(mask, v, base + k);
-        return s;
-    }
-}
 
 template <int n>
 __global__ void __launch_bounds__(kThreads)
@@ -60,7 +44,6 @@ coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_
     const int warp = threadIdx.x >> 5;
     const int g = lane / n;          // token group within the warp
     const int i = lane - g * n;      // row owned by this lane
-    const int base = g * n;
     // lanes of whole groups take part in the shuffles; the spare lanes
     // (32 mod n of them) sit out
     const unsigned mask = kGroups * n == 32 ? 0xFFFFFFFFu : ((1u << (kGroups * n)) - 1u);
@@ -71,41 +54,9 @@ coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_
     const int64_t t = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kGroups + g;
     const bool valid = t < B;
     const int64_t tt = valid ? t : B - 1;  // idle groups mirror the last token, store nothing
-    const float *y = Y + tt * N;
-    const float rb = __ldg(r + tt);
-
-    // §2.3 + §2.4, pre and post entries i
-    const float tp = a_pre * __ldg(y + i) / rb + __ldg(bias + i);
-    const float tq = a_post * __ldg(y + n + i) / rb + __ldg(bias + n + i);
-    const float hp = 1.0f / (1.0f + expf(-tp));
-    const float hq = 2.0f / (1.0f + expf(-tq));
-
-    // §2.4 Sinkhorn–Knopp, row i of the res block
-    float m[n];
-#pragma unroll
-    for (int j = 0; j < n; ++j)
-        m[j] = a_res * __ldg(y + 2 * n + i * n + j) / rb + __ldg(bias + 2 * n + i * n + j);
-    if (iters > 0) {
-        float mx = m[0];
-#pragma unroll
-        for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[j]);
-#pragma unroll
-        for (int j = 0; j < n; ++j) m[j] = expf(m[j] - mx);
-    } else {
-#pragma unroll
-        for (int j = 0; j < n; ++j) m[j] = expf(m[j]);
-    }
-    for (int it = 0; it < iters; ++it) {
-        float s = m[0];
-#pragma unroll
-        for (int j = 1; j < n; ++j) s += m[j];
-        const float inv = __frcp_rn(s);
-#pragma unroll
-        for (int j = 0; j < n; ++j) m[j] *= inv;
-#pragma unroll
-        for (int j = 0; j < n; ++j) m[j] *= __frcp_rn(group_sum<n>(m[j], base, mask));
-    }
-
+    float hp, hq, m[n];
+    coeff_lane<n>(Y + tt * N, __ldg(r + tt), bias, a_pre, a_post, a_res, iters, i, g * n, mask, hp,
+                  hq, m);
     if (valid) {
         H_pre[t * n + i] = hp;
         H_post[t * n + i] = hq;

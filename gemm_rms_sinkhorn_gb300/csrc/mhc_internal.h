@@ -5,6 +5,7 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace mhc {
@@ -53,6 +54,20 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
                             cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
                             int64_t stall_stage = -1);
 cudaError_t read_and_clear_device_status(int *status);
+
+// Tensor map of a 2-D bf16 tensor [rows][cols] (cols contiguous): boxes of
+// box_rows × 64 elements, 128-byte swizzle, zero fill out of bounds.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows);
+
+// ---- steps 1-4a in one persistent kernel, X read once (fused_pre.cu)
+bool fused_pre_eligible(int64_t B, int n, int64_t C, int num_sms);
+size_t fused_pre_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+cudaError_t launch_fused_pre(const uint16_t *X, const uint16_t *phi_t, float a_pre, float a_post,
+                             float a_res, const float *bias, int iters, int64_t B, int n,
+                             int64_t C, float *Y, float *r, float *H_pre, float *H_post,
+                             float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
+                             cudaStream_t stream);
+cudaError_t read_and_clear_fused_status(int *status);
 
 // ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
 cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,

@@ -30,6 +30,25 @@ int mhc_testing_gemm_rms_stalled(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64
                                  size_t workspace_bytes, int64_t stall_stage,
                                  uint64_t wait_limit_ns, mhc_stream_t stream);
 
+/*
+ * mhc_forward with steps 1-4a in one persistent kernel that reads X from HBM
+ * once for both the projection GEMM and the pre-mixing: chunks of token tiles
+ * small enough to stay in L2, several CTAs per tile with a deterministic
+ * fixed-order reduction of their partial sums, and the pre-apply re-reading
+ * each tile's X with bulk copies.  Same arguments, rules, outputs and
+ * tolerances as mhc_forward (the split-K partition differs, so Y differs in
+ * rounding).  Returns MHC_ERR_UNSUPPORTED for shapes the kernel does not take
+ * (fewer than two 128-token tiles, or K too short to split over the CTAs of
+ * a tile).  Measured on GB300 it is not yet faster than mhc_forward: the
+ * second read of X mostly misses L2, so mhc_forward does not use it.
+ */
+int mhc_testing_forward_fused(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                              float alpha_pre, float alpha_post, float alpha_res,
+                              const float *bias, int iters, int64_t B, int n, int64_t C, float *Y,
+                              float *r, float *H_pre, float *H_post, float *H_res,
+                              mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
+                              size_t workspace_bytes, mhc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

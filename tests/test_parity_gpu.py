@@ -201,14 +201,20 @@ def test_post_res_apply_permutation_is_exact():
 # ------------------------------------------------------------ forward
 
 
-def forward_gpu(inp, wl, inplace=False):
+def forward_gpu(inp, wl, inplace=False, fused=False):
     X = dev_bf16(inp["X"])
     B = X.shape[0]
     out = mhc.alloc_outputs(B, wl.n, wl.C)
     if inplace:
         out["X_next"] = X
-    mhc.forward(X, dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), wl.alpha_pre, wl.alpha_post,
-                wl.alpha_res, dev_f32(inp["bias"]), wl.iters, wl.n, wl.C, out=out)
+    args = (X, dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), wl.alpha_pre, wl.alpha_post,
+            wl.alpha_res, dev_f32(inp["bias"]), wl.iters)
+    if fused:
+        mhc.mhc_testing_forward_fused(*args, B, wl.n, wl.C, out["Y"], out["r"], out["H_pre"],
+                                      out["H_post"], out["H_res"], out["F_pre"], out["X_next"],
+                                      out["ws"])
+    else:
+        mhc.forward(*args, wl.n, wl.C, out=out)
     torch.cuda.synchronize()
     return out
 
@@ -271,6 +277,31 @@ def test_forward_prefill_full_size_sampled():
     Y0, X0 = out["Y"].clone(), out["X_next"].clone()
     out2 = forward_gpu(inp, wl)
     assert torch.equal(Y0, out2["Y"]) and torch.equal(X0, out2["X_next"])
+
+
+# shapes for the one-kernel steps 1-4a path (test hook): a ragged last tile, a
+# ragged last chunk of tiles, n=8, a single chunk, and the 7B-width workload
+FUSED_SHAPES = [(1000, 4, 7168), (1100, 4, 4096), (600, 8, 2048), (256, 4, 2048), (4096, 4, 4096)]
+
+
+@pytest.mark.parametrize("B,n,C", FUSED_SHAPES)
+def test_forward_fused_path_shapes(B, n, C):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=6)
+    out = forward_gpu(inp, wl, fused=True)
+    check_forward(out, inp, wl)
+    check_properties(out, wl)
+    again = forward_gpu(inp, wl, fused=True)
+    for k in ("Y", "r", "H_res", "F_pre", "X_next"):
+        assert torch.equal(out[k], again[k]), k  # fixed-order sums: bitwise reproducible
+
+
+def test_forward_fused_path_rejects_one_tile():
+    wl = WORKLOADS["tiny"]
+    inp = make_inputs(wl, seed=6)
+    with pytest.raises(mhc.MhcError) as ei:
+        forward_gpu(inp, wl, fused=True)
+    assert ei.value.status == mhc.MHC_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("B,n,C", ODD_SHAPES)
