@@ -325,6 +325,8 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of identical load kept up for the clock samples")
+    ap.add_argument("--fused", action="store_true",
+                    help="run each step through the one-kernel steps 1-4a test hook")
     ap.add_argument("--mode", default="full", choices=["full", "kernels", "latency"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
                          "latency: microseconds per mhc_forward (stream and CUDA graph)")
@@ -368,11 +370,13 @@ def main() -> int:
     out = mhc.alloc_outputs(B, n, C, dev)
     stream = torch.cuda.current_stream(dev)
 
+    forward_call = mhc.mhc_testing_forward_fused if args.fused else mhc.mhc_forward
+
     def step(on_stream=None):
-        mhc.mhc_forward(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
-                        wl.iters, B, n, C, out["Y"], out["r"], out["H_pre"], out["H_post"],
-                        out["H_res"], out["F_pre"], out["X_next"], out["ws"],
-                        on_stream if on_stream is not None else stream)
+        forward_call(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                     wl.iters, B, n, C, out["Y"], out["r"], out["H_pre"], out["H_post"],
+                     out["H_res"], out["F_pre"], out["X_next"], out["ws"],
+                     on_stream if on_stream is not None else stream)
 
     def barrier():
         if dist is not None:
@@ -391,7 +395,8 @@ def main() -> int:
         res = forward_latency(mhc, step, stream, barrier, args.steps, args.warmup)
         if rank == 0:
             print(json.dumps({"mode": "latency", "workload": wl.name, "B": B, "n": n, "C": C,
-                              **res}), flush=True)
+                              "path": "fused" if args.fused else "mhc_forward", **res}),
+                  flush=True)
         return 0
 
     if args.mode == "kernels":
