@@ -67,6 +67,20 @@ def measured_peaks() -> tuple:
         return FALLBACK_HBM_GBS, "profiling-recipe fallback 6.8 TB/s (of fallback)"
 
 
+def source_digest(kernel: str) -> str:
+    """First 16 hex digits of the SHA-256 over the kernel's .cu file followed by
+    every header under csrc/ (sorted), so a change to shared device code also
+    marks a stored capture as stale."""
+    csrc = os.path.join(ROOT, "gemm_rms_sinkhorn_gb300", "csrc")
+    h = hashlib.sha256()
+    names = [KERNEL_SOURCES[kernel]] + sorted(f for f in os.listdir(csrc)
+                                              if f.endswith((".cuh", ".h")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def stored_traffic(kernel: str):
     """DRAM bytes per launch from a committed ncu capture, or None if stale/absent."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -74,9 +88,7 @@ def stored_traffic(kernel: str):
         with open(path) as f:
             d = json.load(f)
         ent = d[kernel]
-        src = os.path.join(ROOT, "gemm_rms_sinkhorn_gb300", "csrc", KERNEL_SOURCES[kernel])
-        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if ent.get("source_sha256_16") != digest:
+        if ent.get("source_sha256_16") != source_digest(kernel):
             return None
         return int(ent["bytes_per_launch"])
     except Exception:
