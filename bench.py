@@ -337,8 +337,11 @@ def main() -> int:
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of identical load kept up for the clock samples")
-    ap.add_argument("--fused", action="store_true",
-                    help="run each step through the one-kernel steps 1-4a test hook")
+    ap.add_argument("--path", default="auto", choices=["auto", "chain", "decode", "fused"],
+                    help="forward path of each step: auto (mhc_forward's own choice) or one "
+                         "forced through its test hook: chain (four kernels), decode (the "
+                         "small-batch one-launch steps 1-4a), fused (the large-batch one-kernel "
+                         "steps 1-4a)")
     ap.add_argument("--mode", default="full", choices=["full", "kernels", "latency"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
                          "latency: microseconds per mhc_forward (stream and CUDA graph)")
@@ -382,7 +385,9 @@ def main() -> int:
     out = mhc.alloc_outputs(B, n, C, dev)
     stream = torch.cuda.current_stream(dev)
 
-    forward_call = mhc.mhc_testing_forward_fused if args.fused else mhc.mhc_forward
+    forward_call = {"auto": mhc.mhc_forward, "chain": mhc.mhc_testing_forward_chain,
+                    "decode": mhc.mhc_testing_forward_decode,
+                    "fused": mhc.mhc_testing_forward_fused}[args.path]
 
     def step(on_stream=None):
         forward_call(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
@@ -407,7 +412,7 @@ def main() -> int:
         res = forward_latency(mhc, step, stream, barrier, args.steps, args.warmup)
         if rank == 0:
             print(json.dumps({"mode": "latency", "workload": wl.name, "B": B, "n": n, "C": C,
-                              "path": "fused" if args.fused else "mhc_forward", **res}),
+                              "path": args.path, **res}),
                   flush=True)
         return 0
 

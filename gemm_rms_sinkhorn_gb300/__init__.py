@@ -52,6 +52,15 @@ _SIGS = {
                                       ctypes.c_uint64, _vp], _i32),
     "mhc_testing_forward_fused": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_testing_forward_chain": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_testing_forward_decode": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32,
+                                    _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp],
+                                   _i32),
+    "mhc_testing_forward_decode_stalled": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64,
+                                            _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                            _sz, _vp, ctypes.c_uint64], _i32),
+    "mhc_testing_recip": ([_vp, _vp, _i64, _vp], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -148,30 +157,61 @@ def mhc_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, stream=None):
            "mhc_post_res_apply")
 
 
-def mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
-                Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+def _forward_like(name, X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                  Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream, *extra):
     bf, f = torch.bfloat16, torch.float32
     p, nb = _ws(ws)
-    _check(_lib.mhc_forward(_ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), _ptr(F_out, bf, "F_out"),
-                            alpha_pre, alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n,
-                            C, _ptr(Y, f, "Y"), _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"),
-                            _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"),
-                            _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
-                            _stream(stream)),
-           "mhc_forward")
-
-
-def mhc_testing_forward_fused(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B,
-                              n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
-    """Test hook: mhc_forward through the one-kernel steps 1-4a path."""
-    bf, f = torch.bfloat16, torch.float32
-    p, nb = _ws(ws)
-    _check(_lib.mhc_testing_forward_fused(
+    _check(getattr(_lib, name)(
         _ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), _ptr(F_out, bf, "F_out"), alpha_pre,
         alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n, C, _ptr(Y, f, "Y"),
         _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"), _ptr(H_post, f, "H_post"),
         _ptr(H_res, f, "H_res"), _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
-        _stream(stream)), "mhc_testing_forward_fused")
+        _stream(stream), *extra), name)
+
+
+def mhc_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    _forward_like("mhc_forward", X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters,
+                  B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream)
+
+
+def mhc_testing_forward_fused(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B,
+                              n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    """Test hook: mhc_forward through the one-kernel steps 1-4a path for large batches."""
+    _forward_like("mhc_testing_forward_fused", X, phi_t, F_out, alpha_pre, alpha_post, alpha_res,
+                  bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream)
+
+
+def mhc_testing_forward_chain(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B,
+                              n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    """Test hook: mhc_forward through the four-kernel chain whatever the batch."""
+    _forward_like("mhc_testing_forward_chain", X, phi_t, F_out, alpha_pre, alpha_post, alpha_res,
+                  bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream)
+
+
+def mhc_testing_forward_decode(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters,
+                               B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws,
+                               stream=None):
+    """Test hook: mhc_forward through the small-batch one-launch path (B <= 512)."""
+    _forward_like("mhc_testing_forward_decode", X, phi_t, F_out, alpha_pre, alpha_post,
+                  alpha_res, bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws,
+                  stream)
+
+
+def mhc_testing_forward_decode_stalled(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias,
+                                       iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next,
+                                       ws, wait_limit_ns, stream=None):
+    """Test hook: the small-batch path with a grid barrier that never completes."""
+    _forward_like("mhc_testing_forward_decode_stalled", X, phi_t, F_out, alpha_pre, alpha_post,
+                  alpha_res, bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws,
+                  stream, wait_limit_ns)
+
+
+def mhc_testing_recip(x, out, stream=None):
+    """Test hook: the reciprocal the Sinkhorn normalisations and sigmoids use, of each x."""
+    f = torch.float32
+    _check(_lib.mhc_testing_recip(_ptr(x, f, "x"), _ptr(out, f, "out"), x.numel(),
+                                  _stream(stream)), "mhc_testing_recip")
 
 
 def mhc_gemm_rms_noalloc(X, phi_t, B, n, C, Y, r, stream=None):

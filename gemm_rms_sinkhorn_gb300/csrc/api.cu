@@ -1,6 +1,6 @@
 // C ABI of the mHC forward library (declared in include/mhc.h): argument
-// validation on the host, then the kernels of gemm_rms.cu, coeffs.cu and
-// apply.cu on the caller's stream.  No exception crosses this boundary and
+// validation on the host, then the kernels of gemm_rms.cu, coeffs.cu,
+// apply.cu and decode_pre.cu on the caller's stream.  No exception crosses this boundary and
 // nothing here allocates device memory.
 #include <cuda_runtime.h>
 
@@ -114,13 +114,28 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA
 
 size_t bf16_bytes(int64_t count) { return static_cast<size_t>(count) * 2; }
 
-// Workspace of either forward path (and of mhc_gemm_rms), whichever is larger.
+// Workspace of every forward path (and of mhc_gemm_rms), whichever is largest.
 size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
 {
-    const size_t a = gemm_rms_workspace_bytes(B, n, C, num_sms);
-    const size_t b = fused_pre_workspace_bytes(B, n, C, num_sms);
-    return a > b ? a : b;
+    size_t w = gemm_rms_workspace_bytes(B, n, C, num_sms);
+    const size_t f = fused_pre_workspace_bytes(B, n, C, num_sms);
+    const size_t d = decode_pre_workspace_bytes(B, n, C, num_sms);
+    if (f > w) w = f;
+    if (d > w) w = d;
+    return w;
 }
+
+// Batches up to this size take the one-launch steps 1-4a kernel: there the
+// forward is bound by launch and reduction latency, not by HBM.
+constexpr int64_t kDecodeMaxTokens = 128;
+
+enum class Path {
+    Auto,           // decode_pre for small batches, else the four-kernel chain
+    Chain,          // gemm_rms, coeffs, pre_apply
+    Fused,          // fused_pre (test hook)
+    Decode,         // decode_pre (test hook for any eligible batch)
+    DecodeStalled,  // decode_pre whose grid barrier never completes (test hook)
+};
 size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 
 #define MHC_TRY(expr)                   \
@@ -139,7 +154,7 @@ static int forward_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_b
                            int iters, int64_t B, int n, int64_t C, float *Y, float *r,
                            float *H_pre, float *H_post, float *H_res, mhc_bf16 *F_pre,
                            mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,
-                           mhc_stream_t stream, bool use_fused)
+                           mhc_stream_t stream, Path path, uint64_t wait_limit_ns = kWaitLimitNs)
 {
     MHC_TRY(check_shape(B, n, C, true));
     if (iters < 0) return MHC_ERR_INVALID;
@@ -164,11 +179,18 @@ static int forward_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_b
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (use_fused) {
+    if (path == Path::Auto)
+        path = B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C) ? Path::Decode : Path::Chain;
+    if (path == Path::Fused) {
         if (!fused_pre_eligible(B, n, C, info.num_sms)) return MHC_ERR_UNSUPPORTED;
         // steps 1-4a in one kernel that reads X from HBM once
         e = launch_fused_pre(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y,
                              r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s);
+    } else if (path == Path::Decode || path == Path::DecodeStalled) {
+        if (!decode_pre_eligible(B, n, C)) return MHC_ERR_UNSUPPORTED;
+        e = launch_decode_pre(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y,
+                              r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
+                              wait_limit_ns, path == Path::DecodeStalled ? 1 : 0);
     } else {
         e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
         if (e == cudaSuccess)
@@ -310,28 +332,67 @@ int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
 {
     return forward_checked(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
                            C, Y, r, H_pre, H_post, H_res, F_pre, X_next, workspace,
-                           workspace_bytes, stream, false);
+                           workspace_bytes, stream, Path::Auto);
 }
 
-int mhc_testing_forward_fused(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
-                              float alpha_pre, float alpha_post, float alpha_res,
-                              const float *bias, int iters, int64_t B, int n, int64_t C, float *Y,
-                              float *r, float *H_pre, float *H_post, float *H_res,
-                              mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
-                              size_t workspace_bytes, mhc_stream_t stream)
+#define MHC_FORWARD_ARGS                                                                         \
+    const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out, float alpha_pre,            \
+        float alpha_post, float alpha_res, const float *bias, int iters, int64_t B, int n,       \
+        int64_t C, float *Y, float *r, float *H_pre, float *H_post, float *H_res,                \
+        mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,              \
+        mhc_stream_t stream
+#define MHC_FORWARD_PASS                                                                         \
+    X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y, r, H_pre,        \
+        H_post, H_res, F_pre, X_next, workspace, workspace_bytes, stream
+
+int mhc_testing_forward_fused(MHC_FORWARD_ARGS)
 {
-    return forward_checked(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
-                           C, Y, r, H_pre, H_post, H_res, F_pre, X_next, workspace,
-                           workspace_bytes, stream, true);
+    return forward_checked(MHC_FORWARD_PASS, Path::Fused);
+}
+
+int mhc_testing_forward_chain(MHC_FORWARD_ARGS)
+{
+    return forward_checked(MHC_FORWARD_PASS, Path::Chain);
+}
+
+int mhc_testing_forward_decode(MHC_FORWARD_ARGS)
+{
+    return forward_checked(MHC_FORWARD_PASS, Path::Decode);
+}
+
+int mhc_testing_forward_decode_stalled(MHC_FORWARD_ARGS, uint64_t wait_limit_ns)
+{
+    uint64_t lim = wait_limit_ns;
+    if (lim < 1000000ull) lim = 1000000ull;
+    if (lim > kWaitLimitNs) lim = kWaitLimitNs;
+    return forward_checked(MHC_FORWARD_PASS, Path::DecodeStalled, lim);
+}
+
+#undef MHC_FORWARD_ARGS
+#undef MHC_FORWARD_PASS
+
+int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t stream)
+{
+    if (count < 0) return MHC_ERR_INVALID;
+    if (count == 0) return MHC_OK;
+    const Buf ins[] = {{in, f32_bytes(count)}};
+    const Buf outs[] = {{out, f32_bytes(count)}};
+    MHC_TRY(check_ptrs(ins, 1));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 1, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_recip(in, out, count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int mhc_device_status(int *status)
 {
     if (status == nullptr) return MHC_ERR_INVALID;
-    int v = 0, w = 0;
+    int v = 0, w = 0, d = 0;
     if (read_and_clear_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
     if (read_and_clear_fused_status(&w) != cudaSuccess) return MHC_ERR_CUDA;
-    *status = v != MHC_OK ? v : w;
+    if (read_and_clear_decode_status(&d) != cudaSuccess) return MHC_ERR_CUDA;
+    *status = v != MHC_OK ? v : (w != MHC_OK ? w : d);
     return MHC_OK;
 }
 

@@ -66,6 +66,17 @@ post_res_apply_kernel(const uint16_t *X, const uint16_t *__restrict__ F_out,
     ptx::pdl_wait();  // H_res and H_post come from earlier kernels
     ptx::pdl_trigger();
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        // the token's X and F_out are requested (into L2, no registers held)
+        // before its coefficients, so the two round trips overlap; wider n has
+        // no registers to spare for the addresses under its 128-register cap
+        if constexpr (n <= 4) {
+            if (c8 < C8) {
+                const uint16_t *x = X + b * n * C + c8 * 8;
+#pragma unroll
+                for (int j = 0; j < n; ++j) ptx::prefetch_l2(x + j * C);
+                ptx::prefetch_l2(F_out + b * C + c8 * 8);
+            }
+        }
         __syncthreads();  // previous token's coefficients are no longer read
         for (int t = threadIdx.x; t < n * n + n; t += blockDim.x)
             hs[t] = t < n * n ? __ldg(H_res + b * n * n + t) : __ldg(H_post + b * n + (t - n * n));
@@ -80,22 +91,7 @@ post_res_apply_kernel(const uint16_t *X, const uint16_t *__restrict__ F_out,
             unpack8(fv, f);
             uint16_t *y = X_next + b * n * C + c8 * 8;
 #pragma unroll
-            for (int i = 0; i < n; ++i) {
-                float acc[8], t[8];
-                const float hp = hs[n * n + i];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = 0.f;
-#pragma unroll
-                for (int j = 0; j < n; ++j) {
-                    const float hij = hs[i * n + j];
-                    unpack8(xv[j], t);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) acc[e] = fmaf(hij, t[e], acc[e]);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[e] = fmaf(hp, f[e], acc[e]);
-                ptx::st_stream_v4(y + i * C, pack8(acc));
-            }
+            for (int i = 0; i < n; ++i) ptx::st_stream_v4(y + i * C, post_mix8<n>(hs, i, xv, f));
         }
     }
 }

@@ -6,19 +6,11 @@
 //   H̃ = α_seg·Y/r + b;  H_pre = σ(H̃_pre);  H_post = 2σ(H̃_post)
 //   H_res = exp(H̃_res), then `iters` × (rows /= row sums; columns /= column sums)
 //
-// A token is handled by a group of n consecutive lanes of a warp; lane i of
-// the group owns row i of the n×n block (in registers) and entry i of the pre
-// and post segments.  Row sums are lane-local; column sums are a shuffle
-// reduction across the group that every lane evaluates in the same order, so
-// all lanes divide a column by the identical sum.  Each normalisation takes
-// one correctly rounded reciprocal per sum and multiplies by it (at most one
-// rounding away from a true division).  Spreading a token over n lanes gives
-// the serial iteration n times more warps to hide its latency.
-//
-// Before the first row normalisation each row is shifted by its maximum:
-// exp(h - m)/Σ exp(h - m) = exp(h)/Σ exp(h), so every iterate from the first
-// row step on is unchanged in exact arithmetic while exp cannot overflow.
-// With iters = 0 the raw exp(H̃_res) is returned and no shift is applied.
+// One thread per token holds the whole n×n block in registers (token_coeffs),
+// so the iteration needs no communication between threads and its latency is
+// one thread's dependency chain: the n row (then column) sums of a step are
+// independent and overlap.  Y rows are read with 128-bit loads when N keeps
+// them 16-byte aligned (n even).
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -30,7 +22,7 @@
 namespace mhc {
 namespace {
 
-constexpr int kThreads = 128;
+constexpr int kThreads = 64;  // small blocks spread a mid-size batch over more SMs
 
 template <int n>
 __global__ void __launch_bounds__(kThreads)
@@ -39,30 +31,26 @@ coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_
               float *__restrict__ H_pre, float *__restrict__ H_post, float *__restrict__ H_res)
 {
     constexpr int N = n * n + 2 * n;
-    constexpr int kGroups = 32 / n;  // tokens per warp
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int g = lane / n;          // token group within the warp
-    const int i = lane - g * n;      // row owned by this lane
-    // lanes of whole groups take part in the shuffles; the spare lanes
-    // (32 mod n of them) sit out
-    const unsigned mask = kGroups * n == 32 ? 0xFFFFFFFFu : ((1u << (kGroups * n)) - 1u);
-    if (g >= kGroups) return;
     ptx::pdl_wait();  // Y and r come from the previous kernel
     ptx::pdl_trigger();
-
-    const int64_t t = (static_cast<int64_t>(blockIdx.x) * (kThreads / 32) + warp) * kGroups + g;
-    const bool valid = t < B;
-    const int64_t tt = valid ? t : B - 1;  // idle groups mirror the last token, store nothing
-    float hp, hq, m[n];
-    coeff_lane<n>(Y + tt * N, __ldg(r + tt), bias, a_pre, a_post, a_res, iters, i, g * n, mask, hp,
-                  hq, m);
-    if (valid) {
-        H_pre[t * n + i] = hp;
-        H_post[t * n + i] = hq;
-        float *o = H_res + t * n * n + i * n;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < B;
+         t += stride) {
+        float y[N];
+        if constexpr (N % 4 == 0) {
+            const float4 *src = reinterpret_cast<const float4 *>(Y + t * N);
 #pragma unroll
-        for (int j = 0; j < n; ++j) o[j] = m[j];
+            for (int k = 0; k < N / 4; ++k) {
+                const float4 v = __ldg(src + k);
+                y[4 * k] = v.x; y[4 * k + 1] = v.y; y[4 * k + 2] = v.z; y[4 * k + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < N; ++k) y[k] = __ldg(Y + t * N + k);
+        }
+        float hp[n], hq[n], m[n][n];
+        token_coeffs<n>(y, __ldg(r + t), bias, a_pre, a_post, a_res, iters, hp, hq, m);
+        store_token_coeffs<n>(t, hp, hq, m, H_pre, H_post, H_res);
     }
 }
 
@@ -71,13 +59,29 @@ cudaError_t launch_n(const float *Y, const float *r, float a_pre, float a_post, 
                      const float *bias, int iters, int64_t B, float *H_pre, float *H_post,
                      float *H_res, cudaStream_t stream)
 {
-    constexpr int64_t tokens_per_block = (kThreads / 32) * (32 / n);
-    const int64_t blocks = (B + tokens_per_block - 1) / tokens_per_block;
+    const int64_t need = (B + kThreads - 1) / kThreads;
+    const int64_t blocks = need < (int64_t{1} << 20) ? need : (int64_t{1} << 20);
     return launch_pdl(coeffs_kernel<n>, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0,
                       stream, Y, r, a_pre, a_post, a_res, bias, iters, B, H_pre, H_post, H_res);
 }
 
+__global__ void recip_kernel(const float *__restrict__ in, float *__restrict__ out, int64_t count)
+{
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+         i += stride)
+        out[i] = recip_approx(in[i]);
+}
+
 }  // namespace
+
+cudaError_t launch_recip(const float *in, float *out, int64_t count, cudaStream_t stream)
+{
+    const int64_t need = (count + 255) / 256;
+    const int blocks = static_cast<int>(need < 4096 ? need : 4096);
+    recip_kernel<<<blocks, 256, 0, stream>>>(in, out, count);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,
                           const float *bias, int iters, int64_t B, int n, float *H_pre,

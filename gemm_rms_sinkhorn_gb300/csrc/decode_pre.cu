@@ -1,0 +1,424 @@
+// Steps 1 to 4a of the mHC forward in one launch for small batches (decode):
+// the projection GEMM with the RMS (§2.1, §2.2), the coefficients and the
+// Sinkhorn–Knopp projection (§2.3, §2.4), and F_pre (§2.5 (1)), page "mHC 算法
+// 分析 & cutile 高效实现".  With a few tokens the forward is a chain of
+// latencies, not of bytes (§3.2 counts the launches, §5.1 the idle SMs), so
+// this kernel replaces four launches by one and spreads the GEMM over every SM.
+//
+//   phase 1  the stream-K X·φ + Σx² pipeline of gemm_pipeline.cuh over all SMs;
+//            every CTA parks its partial sums (one slot per CTA and token tile);
+//   barrier  a grid-wide arrival count (the launch is cooperative, so every CTA
+//            is resident), bounded like every other wait;
+//   phase 2  CTA c owns the items [c·T/G, (c+1)·T/G) of the T = B·C/8 pieces
+//            of 8 channels, token-major.  For each token its items touch it
+//            sums the partials over the tile's contributors in a fixed order
+//            (segments of 32 contributors in index order, then the segments in
+//            index order), so every CTA that needs a token gets the same bits,
+//            then runs token_coeffs (one thread per token); the CTA owning the
+//            token's first item writes Y, r, H_pre, H_post and H_res;
+//   phase 3  F_pre of its items from X, which phase 1 has just streamed
+//            through L2, by nine warps while the tenth runs the Sinkhorn
+//            iteration (F_pre needs only H_pre, a sigmoid of the totals).
+// X_next (§2.5 (2)) needs F_out, which in a layer only exists after F has run
+// on F_pre, so it stays a launch of its own (apply.cu).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gemm_pipeline.cuh"
+#include "mhc_internal.h"
+#include "mix.cuh"
+#include "ptx.cuh"
+
+namespace mhc {
+namespace {
+
+using pipe::kBK;
+using pipe::kBM;
+using pipe::Sched;
+using pipe::Segment;
+using pipe::SegIter;
+
+constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
+constexpr int kRingBudget = 160 * 1024;
+constexpr int kMaxTokens = 512;   // largest batch this path takes
+constexpr int kSegLen = 32;       // contributors per first-level segment of the sum
+constexpr int kRedFloats = 16384; // first-level segment sums of one token batch
+constexpr int kTokBatch = 32;     // tokens whose coefficients are formed together
+
+__device__ int g_decode_status;
+
+constexpr int npad_for(int n) { return (n * n + 2 * n + 15) / 16 * 16; }
+
+template <int n>
+struct DCfg {
+    static constexpr int N = n * n + 2 * n;
+    static constexpr int V = N + 1;  // a partial row: N sums of products, then Σx²
+    static constexpr int NPAD = npad_for(n);
+    using C = pipe::Cfg<NPAD, kRingBudget>;
+    static constexpr int kBiasBytes = (N * 4 + 15) / 16 * 16;  // b, staged for phase 2
+    static constexpr int kSmemBytes =
+        1024 + C::kRingBytes + pipe::kSsBytes + pipe::kBarrierBytes + kBiasBytes;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+    // phase 2 scratch reuses the stage ring
+    static_assert((kRedFloats + kTokBatch * V + kTokBatch * n + kTokBatch * 4) * 4 <=
+                      C::kRingBytes, "scratch");
+};
+
+constexpr int kMaxTiles = kMaxTokens / kBM;
+
+// The contributors (CTAs) first[m]..last[m] of each token tile, from the host.
+struct TileCtas {
+    int first[kMaxTiles], last[kMaxTiles];
+};
+
+// Bounded spin until *ctr >= target; false when the limit ran out.
+__device__ bool wait_arrivals(const uint32_t *ctr, uint32_t target, uint64_t limit_ns)
+{
+    const uint64_t t0 = ptx::globaltimer_ns();
+    for (uint32_t polls = 0;; ++polls) {
+        if (ptx::ld_acquire_gpu(ctr) >= target) return true;
+        if ((polls & 31) == 31 && ptx::globaltimer_ns() - t0 > limit_ns) return false;
+        __nanosleep(32);
+    }
+}
+
+template <int n>
+__global__ void __launch_bounds__(kThreads, 1)
+decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
+                  const __grid_constant__ CUtensorMap tm_w, const uint16_t *__restrict__ X,
+                  int64_t B, int64_t C, Sched sch, const __grid_constant__ TileCtas tc,
+                  int seg_max, float a_pre, float a_post, float a_res,
+                  const float *__restrict__ bias, int iters, float *__restrict__ Y,
+                  float *__restrict__ r, float *__restrict__ H_pre, float *__restrict__ H_post,
+                  float *__restrict__ H_res, uint16_t *__restrict__ F_pre,
+                  float *__restrict__ partials, uint32_t *grid_bar, uint32_t bar_target,
+                  uint64_t wait_limit_ns)
+{
+    using D = DCfg<n>;
+    using Cf = typename D::C;
+    constexpr int N = D::N, V = D::V, NPAD = D::NPAD;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    pipe::Pipe p;
+    float *bias_s = reinterpret_cast<float *>(
+        pipe::carve<NPAD, kRingBudget>(p, smem, &g_decode_status, wait_limit_ns));
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int64_t K = n * C;
+    // this CTA's items for phases 2-3 (64-bit divisions: done here, before the
+    // previous kernel has finished, not on the path after the grid barrier)
+    const int64_t C8 = C >> 3;
+    const int64_t T = B * C8;
+    const int64_t lo = T * cta / sch.grid, hi = T * (cta + 1) / sch.grid;
+    const int64_t t_first = lo / C8, t_last = (hi - 1) / C8;
+
+    if (threadIdx.x == 0) {
+        pipe::init_barriers(p);
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_x);
+        ptx::prefetch_tensormap(&tm_w);
+    }
+    if (warp == 1) ptx::tmem_alloc<Cf::kTmemCols>(p.tmem_holder);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    p.tmem_base = *p.tmem_holder;
+    ptx::pdl_wait();
+    // b for phase 2, fetched now so its latency hides behind phase 1
+    for (int k = threadIdx.x; k < N; k += kThreads) bias_s[k] = __ldg(bias + k);
+
+    // ------------------------------------------------------------ phase 1
+    const SegIter segs{sch.lo(cta), sch.lo(cta + 1), sch.kbt};
+    if (warp == 0) {
+        if (lane == 0)  // X is read again in phase 3 and by the X_next kernel: keep it in L2
+            pipe::producer<NPAD>(p, segs, &tm_x, &tm_w, ptx::policy_evict_normal(), -1);
+    } else if (warp == 1) {
+        if (lane == 0) pipe::mma_issuer<NPAD>(p, segs);
+    } else if (warp < 6) {
+        pipe::square_sum<NPAD>(p, segs, (warp - 2) * 32 + lane, lane);
+    } else {
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        int seg = 0;
+        SegIter it = segs;
+        Segment sg;
+        while (it.next(sg)) {
+            float v[NPAD];
+            float ss;
+            if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
+            ++seg;
+            const int64_t grow = static_cast<int64_t>(sg.m) * kBM + row;
+            if (grow < B) {
+                float *mine = partials + (static_cast<int64_t>(cta + sg.m) * kBM + row) * V;
+#pragma unroll
+                for (int j = 0; j < NPAD; ++j)
+                    if (j < N) mine[j] = v[j];
+                mine[N] = ss;
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<Cf::kTmemCols>(p.tmem_base);
+    }
+
+    // ------------------------------------------------------ grid barrier
+    // The CTA barrier above orders every thread's partial stores before thread
+    // 0's fence, which is cumulative: they are visible before its arrival.
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(grid_bar, 1u);
+        if (!*p.abort && !wait_arrivals(grid_bar, bar_target, wait_limit_ns)) pipe::raise_timeout(p);
+    }
+    __syncthreads();
+    if (*p.abort) return;
+    // the X_next kernel may start launching; it waits for this grid to finish
+    ptx::pdl_trigger();
+
+    // -------------------------------------------------- phases 2 and 3
+    if (lo >= hi) return;
+    float *red = reinterpret_cast<float *>(p.stages);  // [seg_max][tokens · V]
+    float *yv = red + kRedFloats;                      // [tokens][V]: Y row, then r
+    float *hps = yv + kTokBatch * V;                   // [tokens][n]: H_pre
+    int *tinfo = reinterpret_cast<int *>(hps + kTokBatch * n);  // [tokens]: first, last, m, row
+    int nb = kRedFloats / (V * seg_max);
+    if (nb > kTokBatch) nb = kTokBatch;
+    for (int64_t t0 = t_first; t0 <= t_last; t0 += nb) {
+        const int cnt = static_cast<int>(t_last - t0 + 1 < nb ? t_last - t0 + 1 : nb);
+        if (threadIdx.x < cnt) {
+            const int64_t t = t0 + threadIdx.x;
+            const int m = static_cast<int>(t / kBM);
+            int *ti = tinfo + threadIdx.x * 4;
+            ti[0] = tc.first[m];
+            ti[1] = tc.last[m];
+            ti[2] = m;
+            ti[3] = static_cast<int>(t - static_cast<int64_t>(m) * kBM);
+        }
+        __syncthreads();
+        // first level: segment s of value v of token j sums contributors
+        // first + s·kSegLen ... (at most kSegLen of them) in index order.  The
+        // value index varies fastest across threads, so a warp's loads of one
+        // contributor are one contiguous partial row.
+        const int Q = cnt * V;
+        const int pairs = Q * seg_max;
+        for (int pi = threadIdx.x; pi < pairs; pi += kThreads) {
+            const int s = pi / Q, qv = pi - s * Q;
+            const int j = qv / V, v = qv - j * V;
+            const int *ti = tinfo + j * 4;
+            const int last = ti[1], m = ti[2], row = ti[3];
+            const int c0 = ti[0] + s * kSegLen;
+            float acc = 0.f;
+            if (c0 <= last) {
+                float vals[kSegLen];
+#pragma unroll
+                for (int u = 0; u < kSegLen; ++u)
+                    vals[u] = c0 + u <= last
+                                  ? __ldcg(partials + (static_cast<int64_t>(c0 + u + m) * kBM + row) * V + v)
+                                  : 0.f;
+                acc = vals[0];
+#pragma unroll
+                for (int u = 1; u < kSegLen; ++u) acc += vals[u];
+            }
+            red[pi] = acc;
+        }
+        __syncthreads();
+        // second level: the segments in index order; Y and r of owned tokens
+        for (int qv = threadIdx.x; qv < cnt * V; qv += kThreads) {
+            const int j = qv / V, v = qv - j * V;
+            const int64_t t = t0 + j;
+            const int segs_t = (tinfo[j * 4 + 1] - tinfo[j * 4] + kSegLen) / kSegLen;
+            float tot = red[qv];
+            for (int s = 1; s < segs_t; ++s) tot += red[s * cnt * V + qv];
+            const bool owner = t * C8 >= lo;  // this CTA holds the token's first item
+            if (v < N) {
+                yv[qv] = tot;
+                if (owner) Y[t * N + v] = tot;
+            } else {
+                const float rr = sqrtf(tot / static_cast<float>(K));
+                yv[qv] = rr;
+                if (owner) r[t] = rr;
+            }
+        }
+        __syncthreads();
+        // H_pre first (σ of the pre entries only), so that F_pre can be formed
+        // while the Sinkhorn iteration runs; token_coeffs forms the same bits
+        if (threadIdx.x < cnt * n) {
+            const int j = threadIdx.x / n, i = threadIdx.x - j * n;
+            hps[threadIdx.x] = pre_coeff(yv[j * V + i], 1.0f / yv[j * V + N], a_pre, bias_s[i]);
+        }
+        __syncthreads();
+        if (warp == kThreads / 32 - 1) {
+            // coefficients, one lane per token (cnt <= kTokBatch = 32)
+            if (lane < cnt) {
+                const int64_t t = t0 + lane;
+                float hp[n], hq[n], mres[n][n];
+                token_coeffs<n>(yv + lane * V, yv[lane * V + N], bias_s, a_pre, a_post, a_res,
+                                iters, hp, hq, mres);
+                if (t * C8 >= lo) store_token_coeffs<n>(t, hp, hq, mres, H_pre, H_post, H_res);
+            }
+        } else {
+            // F_pre of this CTA's items of these tokens, token by token
+            constexpr int kMixThreads = kThreads - 32;
+            for (int j = 0; j < cnt; ++j) {
+                const int64_t t = t0 + j;
+                const int64_t a = t * C8 > lo ? t * C8 : lo;
+                const int64_t b = (t + 1) * C8 < hi ? (t + 1) * C8 : hi;
+                float h[n];
+#pragma unroll
+                for (int i = 0; i < n; ++i) h[i] = hps[j * n + i];
+                for (int64_t c8 = a - t * C8 + threadIdx.x; c8 < b - t * C8; c8 += kMixThreads) {
+                    const uint16_t *x = X + t * n * C + c8 * 8;
+                    uint4 xv[n];
+#pragma unroll
+                    for (int i = 0; i < n; ++i)
+                        xv[i] = __ldg(reinterpret_cast<const uint4 *>(x + i * C));
+                    ptx::st_stream_v4(F_pre + t * C + c8 * 8, pre_mix8<n>(h, xv));
+                }
+            }
+        }
+        __syncthreads();  // the scratch is reused by the next token batch
+    }
+}
+
+// Clears the grid-barrier word before the kernel that counts on it.
+__global__ void zero_word_kernel(uint32_t *w)
+{
+    ptx::pdl_wait();
+    ptx::pdl_trigger();
+    *w = 0;
+}
+
+Sched decode_sched(int64_t B, int n, int64_t C, int num_sms)
+{
+    Sched s;
+    s.m_tiles = static_cast<int>((B + kBM - 1) / kBM);
+    s.kbt = static_cast<int>((n * C + kBK - 1) / kBK);
+    s.total = static_cast<int64_t>(s.m_tiles) * s.kbt;
+    s.grid = static_cast<int>(s.total < num_sms ? s.total : num_sms);
+    return s;
+}
+
+TileCtas tile_ctas(const Sched &s)
+{
+    TileCtas tc{};
+    for (int m = 0; m < s.m_tiles; ++m) {
+        tc.first[m] = s.owner(static_cast<int64_t>(m) * s.kbt);
+        tc.last[m] = s.owner(static_cast<int64_t>(m + 1) * s.kbt - 1);
+    }
+    return tc;
+}
+
+// Largest number of kSegLen-contributor segments of any tile.
+int decode_seg_max(const Sched &s, const TileCtas &tc)
+{
+    int mx = 1;
+    for (int m = 0; m < s.m_tiles; ++m) {
+        const int segs = (tc.last[m] - tc.first[m] + kSegLen) / kSegLen;
+        if (segs > mx) mx = segs;
+    }
+    return mx;
+}
+
+constexpr size_t kBarBytes = 256;
+
+template <int n>
+cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_t *X, int64_t B,
+                     int64_t C, const Sched &s, const TileCtas &tc, int seg_max, float a_pre,
+                     float a_post,
+                     float a_res, const float *bias, int iters, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, uint16_t *F_pre, float *partials,
+                     uint32_t *bar, uint32_t bar_target, uint64_t limit, int device,
+                     cudaStream_t stream)
+{
+    using D = DCfg<n>;
+    static uint64_t configured = 0;  // one bit per device
+    static std::mutex mu;
+    if (device < 64 && !((configured >> device) & 1)) {
+        std::lock_guard<std::mutex> lock(mu);
+        cudaError_t e = cudaFuncSetAttribute(decode_pre_kernel<n>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             D::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured |= 1ull << device;
+    }
+    return launch_coop_pdl(decode_pre_kernel<n>, dim3(s.grid), dim3(kThreads), D::kSmemBytes,
+                           stream, tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias,
+                           iters,
+                           Y, r, H_pre, H_post, H_res, F_pre, partials, bar, bar_target, limit);
+}
+
+}  // namespace
+
+bool decode_pre_eligible(int64_t B, int n, int64_t C)
+{
+    return B >= 1 && B <= kMaxTokens && n >= 1 && n <= 8 && C >= 8 && C % 8 == 0;
+}
+
+size_t decode_pre_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
+{
+    if (!decode_pre_eligible(B, n, C)) return 0;
+    const Sched s = decode_sched(B, n, C, num_sms);
+    const size_t slots = static_cast<size_t>(s.grid) + s.m_tiles;
+    return kBarBytes + slots * kBM * (num_coeffs(n) + 1) * sizeof(float);
+}
+
+cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_pre, float a_post,
+                              float a_res, const float *bias, int iters, int64_t B, int n,
+                              int64_t C, float *Y, float *r, float *H_pre, float *H_post,
+                              float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
+                              cudaStream_t stream, uint64_t wait_limit_ns, int barrier_extra)
+{
+    if (!decode_pre_eligible(B, n, C)) return cudaErrorInvalidValue;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Sched s = decode_sched(B, n, C, num_sms);
+    const TileCtas tc = tile_ctas(s);
+    const int seg_max = decode_seg_max(s, tc);
+    CUtensorMap tx, tw;
+    if (!make_tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
+        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                   static_cast<uint32_t>(npad_for(n))))
+        return cudaErrorInvalidValue;
+    uint32_t *bar = static_cast<uint32_t *>(workspace);
+    float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kBarBytes);
+    cudaError_t e = launch_pdl(zero_word_kernel, dim3(1), dim3(1), 0, stream, bar);
+    if (e != cudaSuccess) return e;
+    int device = 0;
+    if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    const uint32_t target = static_cast<uint32_t>(s.grid + (barrier_extra > 0 ? barrier_extra : 0));
+    switch (n) {
+#define MHC_CASE(k)                                                                            \
+    case k:                                                                                    \
+        return launch_n<k>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias, iters,  \
+                           Y, r,                                                                \
+                           H_pre, H_post, H_res, F_pre, partials, bar, target, wait_limit_ns,   \
+                           device, stream);
+        MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
+        MHC_CASE(8)
+#undef MHC_CASE
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t read_and_clear_decode_status(int *status)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    int v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_decode_status, sizeof v)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_decode_status, &zero, sizeof zero)) != cudaSuccess) return e;
+    *status = v;
+    return cudaSuccess;
+}
+
+}  // namespace mhc

@@ -24,7 +24,7 @@
 //   warps 10-13 pre-apply: H_pre of the rows (σ only), then F_pre of each
 //               piece from shared memory;
 //   warp 14     coefficients: H_pre, H_post and the Sinkhorn–Knopp H_res of
-//               the rows (coeff_lane, as the standalone kernel), off the
+//               the rows (token_coeffs, as the standalone kernel), off the
 //               critical path.
 // Partial slots alternate between two buffers by chunk parity; before reusing
 // one a CTA waits (bounded) until the readers of two chunks back are done.
@@ -287,7 +287,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             if (pt < nrows * n) {
                 const int tk = pt / n, i = pt - (pt / n) * n;
                 const float *yrow = rows_buf + (rb * kMaxRows + tk) * stride;
-                hp_buf[tk * 8 + i] = pre_coeff(yrow[i], yrow[N], a_pre, bias[i]);
+                hp_buf[tk * 8 + i] = pre_coeff(yrow[i], 1.0f / yrow[N], a_pre, bias[i]);
             }
             if (!pipe::group_sync(p, pre_bar, pre_phase)) break;
             if (lane == 0) ptx::mbar_arrive(&rows_empty[rb]);
@@ -321,9 +321,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
         }
     } else if (warp == 14) {
         // ------------------------------------- coefficients (warp 14)
-        constexpr int kGroups = 32 / n;  // tokens per pass
-        const int gg = lane / n, gi = lane - (lane / n) * n;
-        const unsigned mask = kGroups * n == 32 ? 0xFFFFFFFFu : ((1u << (kGroups * n)) - 1u);
+        // one lane per token (token_coeffs), 32 tokens per pass
         int seg = 0;
         ChunkIter it = segs;
         Segment sg;
@@ -334,23 +332,11 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int nrows = clamp_rows(r0, r1, valid);
             const int rb = seg % kRowBufs;
             if (!pipe::wait(p, &rows_full[rb], (seg / kRowBufs) & 1)) break;
-            if (gg < kGroups) {
-                for (int tk0 = 0; tk0 < nrows; tk0 += kGroups) {
-                    const int tk = tk0 + gg;
-                    const bool has = tk < nrows;
-                    const float *yrow = rows_buf + (rb * kMaxRows + (has ? tk : tk0)) * stride;
-                    float hp, hq, m[n];
-                    coeff_lane<n>(yrow, yrow[N], bias, a_pre, a_post, a_res, iters, gi, gg * n,
-                                  mask, hp, hq, m);
-                    if (has) {
-                        const int64_t tok = row0 + r0 + tk;
-                        H_pre[tok * n + gi] = hp;
-                        H_post[tok * n + gi] = hq;
-                        float *o = H_res + tok * n * n + gi * n;
-#pragma unroll
-                        for (int k = 0; k < n; ++k) o[k] = m[k];
-                    }
-                }
+            for (int tk = lane; tk < nrows; tk += 32) {
+                const float *yrow = rows_buf + (rb * kMaxRows + tk) * stride;
+                float hp[n], hq[n], m[n][n];
+                token_coeffs<n>(yrow, yrow[N], bias, a_pre, a_post, a_res, iters, hp, hq, m);
+                store_token_coeffs<n>(row0 + r0 + tk, hp, hq, m, H_pre, H_post, H_res);
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&rows_empty[rb]);

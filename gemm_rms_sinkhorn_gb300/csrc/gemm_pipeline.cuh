@@ -56,6 +56,36 @@ struct Segment {
     int m, k0, k1;  // token tile, K-block range [k0, k1)
 };
 
+// Static stream-K schedule: the units (token tile, 64-wide K block), ordered
+// tile-major, are split into `grid` equal contiguous ranges; CTA c owns units
+// [lo(c), lo(c+1)).
+struct Sched {
+    int64_t total;  // m_tiles * kbt
+    int kbt;        // K blocks per token tile
+    int m_tiles;
+    int grid;
+    __host__ __device__ int64_t lo(int c) const { return total * c / grid; }
+    // The CTA whose range holds unit u.
+    __host__ __device__ int owner(int64_t u) const {
+        return static_cast<int>(((u + 1) * grid - 1) / total);
+    }
+};
+
+// Walks the segments (one token tile, a contiguous K-block range) of a CTA.
+struct SegIter {
+    int64_t u, end;
+    int kbt;
+    __device__ bool next(Segment &s) {
+        if (u >= end) return false;
+        s.m = static_cast<int>(u / kbt);
+        s.k0 = static_cast<int>(u - static_cast<int64_t>(s.m) * kbt);
+        int64_t left = end - u;
+        s.k1 = left < kbt - s.k0 ? s.k0 + static_cast<int>(left) : kbt;
+        u += s.k1 - s.k0;
+        return true;
+    }
+};
+
 // Pointers into one CTA's shared memory plus the per-kernel wait settings.
 struct Pipe {
     uint8_t *stages;

@@ -38,6 +38,8 @@ namespace {
 using pipe::kBK;
 using pipe::kBM;
 using pipe::Segment;
+using pipe::Sched;
+using pipe::SegIter;
 
 constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
 constexpr int kEpiThreads = 128;
@@ -52,34 +54,6 @@ struct KCfg {
     using C = pipe::Cfg<NPAD, kRingBudget>;
     static constexpr int kSmemBytes = 1024 + C::kRingBytes + pipe::kSsBytes + pipe::kBarrierBytes;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
-};
-
-// Static stream-K schedule: CTA c owns units [lo(c), lo(c+1)).
-struct Sched {
-    int64_t total;  // m_tiles * kbt
-    int kbt;        // K blocks per token tile
-    int m_tiles;
-    int grid;
-    __host__ __device__ int64_t lo(int c) const { return total * c / grid; }
-    // The CTA whose range holds unit u.
-    __host__ __device__ int owner(int64_t u) const {
-        return static_cast<int>(((u + 1) * grid - 1) / total);
-    }
-};
-
-// Walks the segments (one token tile, a contiguous K-block range) of a CTA.
-struct SegIter {
-    int64_t u, end;
-    int kbt;
-    __device__ bool next(Segment &s) {
-        if (u >= end) return false;
-        s.m = static_cast<int>(u / kbt);
-        s.k0 = static_cast<int>(u - static_cast<int64_t>(s.m) * kbt);
-        int64_t left = end - u;
-        s.k1 = left < kbt - s.k0 ? s.k0 + static_cast<int>(left) : kbt;
-        u += s.k1 - s.k0;
-        return true;
-    }
 };
 
 template <int NPAD>

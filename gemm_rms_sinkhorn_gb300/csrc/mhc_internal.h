@@ -32,6 +32,27 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// As launch_pdl, and cooperative: every CTA of the grid is resident at once
+// (the launch fails otherwise), so CTAs may wait on one another.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeCooperative;
+    attr[1].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // N = n² + 2n coefficient columns per token.
 inline int num_coeffs(int n) { return n * n + 2 * n; }
 
@@ -69,10 +90,25 @@ cudaError_t launch_fused_pre(const uint16_t *X, const uint16_t *phi_t, float a_p
                              cudaStream_t stream);
 cudaError_t read_and_clear_fused_status(int *status);
 
+// ---- steps 1-4a in one cooperative launch for small batches (decode_pre.cu)
+bool decode_pre_eligible(int64_t B, int n, int64_t C);
+size_t decode_pre_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+// barrier_extra > 0 is a test hook: the grid barrier waits for that many
+// arrivals more than there are CTAs, so every CTA's wait runs out.
+cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_pre, float a_post,
+                              float a_res, const float *bias, int iters, int64_t B, int n,
+                              int64_t C, float *Y, float *r, float *H_pre, float *H_post,
+                              float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
+                              cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
+                              int barrier_extra = 0);
+cudaError_t read_and_clear_decode_status(int *status);
+
 // ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
 cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,
                           const float *bias, int iters, int64_t B, int n, float *H_pre,
                           float *H_post, float *H_res, cudaStream_t stream);
+// Test hook: out[i] = the reciprocal the Sinkhorn normalisations and sigmoids use, of in[i].
+cudaError_t launch_recip(const float *in, float *out, int64_t count, cudaStream_t stream);
 
 // ---- step 4: apply kernels (apply.cu)
 cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, int n, int64_t C,

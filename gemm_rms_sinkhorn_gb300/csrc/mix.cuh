@@ -1,8 +1,9 @@
 // Per-token arithmetic shared by the standalone kernels and the fused one
 // (page "mHC 算法分析 & cutile 高效实现", §2.3–§2.5):
-//   coeff_lane  one lane's share of a token's coefficients: entries i of H_pre
-//               and H_post and row i of the Sinkhorn–Knopp block;
-//   pre_mix8    F_pre for 8 channels of one token from its n streams.
+//   token_coeffs  all of one token's coefficients in one thread (H_pre,
+//                 H_post and the Sinkhorn–Knopp block);
+//   pre_mix8      F_pre for 8 channels of one token from its n streams;
+//   post_mix8     X_next for 8 channels of one token from its n streams.
 #pragma once
 
 #include <cstdint>
@@ -11,66 +12,179 @@
 
 namespace mhc {
 
-// Sum over the n lanes of a token group of v, identical on every lane.
-template <int n>
-__device__ __forceinline__ float group_sum(float v, int base, unsigned mask)
+// 1/s for the Sinkhorn normalisations and the sigmoids: the hardware's
+// approximate reciprocal, within one ulp of the exact 1/s over the normal
+// range (the PTX ISA's bound for rcp.approx; a GPU test checks it), flushing
+// subnormal inputs and results to zero.  The row and column sums are always
+// normal: every row holds its maximum, exp(0) = 1, before the first step.
+// One instruction without a branch, so the n reciprocals of a row or column
+// step overlap, where a correctly rounded division's slow-path branch
+// serialises them.
+__device__ __forceinline__ float recip_approx(float s)
 {
-    if constexpr ((n & (n - 1)) == 0) {
-        // butterfly: a + b == b + a exactly, so every lane ends with the same value
-#pragma unroll
-        for (int off = 1; off < n; off <<= 1) v += __shfl_xor_sync(mask, v, off);
-        return v;
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
+    return y;
+}
+
+// σ(x) = 1/(1 + e^{−x}) with the reciprocal above.  For x below about −88,
+// e^{−x} overflows; the clamp keeps the reciprocal finite, and its value
+// (below the smallest normal float) flushes to the exact limit 0.
+__device__ __forceinline__ float sigmoid(float x)
+{
+    return recip_approx(fminf(1.0f + expf(-x), 3.0e38f));
+}
+
+// §2.3 + §2.4 for one pre entry: H_pre = σ(α_pre·y·(1/r) + b).  inv_r is the
+// token's 1/r; every caller forms it as 1.0f / r, so all get the same bits.
+__device__ __forceinline__ float pre_coeff(float y, float inv_r, float a_pre, float b)
+{
+    return sigmoid(a_pre * y * inv_r + b);
+}
+
+// Σ v[0..k) as a balanced tree (depth ⌈log2 k⌉, which shortens the
+// Sinkhorn step's dependency chain).
+template <int k>
+__device__ __forceinline__ float tree_sum(const float *v)
+{
+    if constexpr (k == 1) {
+        return v[0];
     } else {
-        float s = __shfl_sync(mask, v, base);
-#pragma unroll
-        for (int k = 1; k < n; ++k) s += __shfl_sync(mask, v, base + k);
-        return s;
+        constexpr int h = k / 2;
+        return tree_sum<h>(v) + tree_sum<k - h>(v + h);
     }
 }
 
-// §2.3 + §2.4 for one pre entry: H_pre = σ(α_pre·y/r + b).  The expression
-// leaves the compiler nothing to contract, so every caller gets the same bits.
-__device__ __forceinline__ float pre_coeff(float y, float rb, float a_pre, float b)
-{
-    return 1.0f / (1.0f + expf(-(a_pre * y / rb + b)));
-}
-
-// Lane i of the n-lane group of one token (lanes base..base+n-1 of the warp,
-// all in `mask`).  y: the token's N = n²+2n raw coefficients; rb: its r.
-//   §2.3  H̃ = α_seg·y/r + b
-//   §2.4  hp = σ(H̃_pre[i]), hq = 2σ(H̃_post[i]); m = row i of Sinkhorn(exp H̃_res)
-// The n×n block is row-distributed over the lanes; each normalisation
-// multiplies by one correctly rounded reciprocal of the sum.  Rows are shifted
-// by their maximum before exp when iters > 0 (exact after the first row
-// normalisation); iters = 0 returns the raw exp(H̃_res).
+// All coefficients of one token in one thread.  y: the token's N = n²+2n raw
+// coefficients; rb: its r.
+//   §2.3  H̃ = α_seg·y/r + b, with y/r formed as y·(1/r): one division a token
+//         (a division's slow-path branch keeps n²+2n of them from overlapping)
+//   §2.4  hp = σ(H̃_pre), hq = 2σ(H̃_post); m = Sinkhorn–Knopp(exp H̃_res)
+// The n×n block stays in registers, so row and column sums are thread-local
+// (pairwise tree sums).  Each normalisation multiplies by one reciprocal of
+// the sum.  Rows are shifted by their maximum before exp when iters > 0:
+// exp(h − mx)/Σ exp(h − mx) = exp(h)/Σ exp(h), so every iterate from the first
+// row step on is unchanged in exact arithmetic while exp cannot overflow;
+// iters = 0 returns the raw exp(H̃_res).
 template <int n>
-__device__ __forceinline__ void coeff_lane(const float *y, float rb, const float *bias, float a_pre,
-                                           float a_post, float a_res, int iters, int i, int base,
-                                           unsigned mask, float &hp, float &hq, float (&m)[n])
+__device__ __forceinline__ void token_coeffs(const float *y, float rb, const float *bias,
+                                             float a_pre, float a_post, float a_res, int iters,
+                                             float (&hp)[n], float (&hq)[n], float (&m)[n][n])
 {
-    hp = pre_coeff(y[i], rb, a_pre, bias[i]);
-    hq = 2.0f / (1.0f + expf(-(a_post * y[n + i] / rb + bias[n + i])));
+    const float inv_r = 1.0f / rb;
 #pragma unroll
-    for (int j = 0; j < n; ++j) m[j] = a_res * y[2 * n + i * n + j] / rb + bias[2 * n + i * n + j];
+    for (int i = 0; i < n; ++i) {
+        hp[i] = pre_coeff(y[i], inv_r, a_pre, bias[i]);
+        hq[i] = 2.0f * sigmoid(a_post * y[n + i] * inv_r + bias[n + i]);
+    }
+#pragma unroll
+    for (int i = 0; i < n; ++i)
+#pragma unroll
+        for (int j = 0; j < n; ++j)
+            m[i][j] = a_res * y[2 * n + i * n + j] * inv_r + bias[2 * n + i * n + j];
     if (iters > 0) {
-        float mx = m[0];
 #pragma unroll
-        for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[j]);
+        for (int i = 0; i < n; ++i) {
+            float mx = m[i][0];
 #pragma unroll
-        for (int j = 0; j < n; ++j) m[j] = expf(m[j] - mx);
+            for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[i][j]);
+#pragma unroll
+            for (int j = 0; j < n; ++j) m[i][j] = expf(m[i][j] - mx);
+        }
     } else {
 #pragma unroll
-        for (int j = 0; j < n; ++j) m[j] = expf(m[j]);
+        for (int i = 0; i < n; ++i)
+#pragma unroll
+            for (int j = 0; j < n; ++j) m[i][j] = expf(m[i][j]);
     }
-    for (int it = 0; it < iters; ++it) {
-        float s = m[0];
+    if constexpr (n <= 4) {
+        // rows, then columns, scaled in place
+        for (int it = 0; it < iters; ++it) {
 #pragma unroll
-        for (int j = 1; j < n; ++j) s += m[j];
-        const float inv = __frcp_rn(s);
+            for (int i = 0; i < n; ++i) {
+                const float inv = recip_approx(tree_sum<n>(m[i]));
 #pragma unroll
-        for (int j = 0; j < n; ++j) m[j] *= inv;
+                for (int j = 0; j < n; ++j) m[i][j] *= inv;
+            }
 #pragma unroll
-        for (int j = 0; j < n; ++j) m[j] *= __frcp_rn(group_sum<n>(m[j], base, mask));
+            for (int j = 0; j < n; ++j) {
+                float col[n];
+#pragma unroll
+                for (int i = 0; i < n; ++i) col[i] = m[i][j];
+                const float inv = recip_approx(tree_sum<n>(col));
+#pragma unroll
+                for (int i = 0; i < n; ++i) m[i][j] *= inv;
+            }
+        }
+    } else {
+        // The same iteration kept as diagonal scalings of the fixed A = m:
+        // after each step the iterate is diag(u)·A·diag(v), the row step sets
+        // u_i = 1/Σ_j A_ij·v_j and the column step v_j = 1/Σ_i u_i·A_ij.  It does
+        // no n² rescaling per step, which measured 1.3–2.5× faster per
+        // iteration on GB300 for n = 5..8 (the in-place form is faster at n <= 4).
+        if (iters > 0) {
+            float u[n], v[n];
+#pragma unroll
+            for (int j = 0; j < n; ++j) v[j] = 1.0f;
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+                    float p[n];
+#pragma unroll
+                    for (int j = 0; j < n; ++j) p[j] = m[i][j] * v[j];
+                    u[i] = recip_approx(tree_sum<n>(p));
+                }
+#pragma unroll
+                for (int j = 0; j < n; ++j) {
+                    float p[n];
+#pragma unroll
+                    for (int i = 0; i < n; ++i) p[i] = u[i] * m[i][j];
+                    v[j] = recip_approx(tree_sum<n>(p));
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < n; ++i)
+#pragma unroll
+                for (int j = 0; j < n; ++j) m[i][j] = (u[i] * m[i][j]) * v[j];
+        }
+    }
+}
+
+// Stores one token's coefficients (row-major H_res), 128-bit where the
+// per-token strides keep 16-byte alignment.
+template <int n>
+__device__ __forceinline__ void store_token_coeffs(int64_t t, const float (&hp)[n],
+                                                   const float (&hq)[n], const float (&m)[n][n],
+                                                   float *H_pre, float *H_post, float *H_res)
+{
+    if constexpr (n % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < n; i += 4) {
+            *reinterpret_cast<float4 *>(H_pre + t * n + i) =
+                make_float4(hp[i], hp[i + 1], hp[i + 2], hp[i + 3]);
+            *reinterpret_cast<float4 *>(H_post + t * n + i) =
+                make_float4(hq[i], hq[i + 1], hq[i + 2], hq[i + 3]);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+            H_pre[t * n + i] = hp[i];
+            H_post[t * n + i] = hq[i];
+        }
+    }
+    float *o = H_res + t * n * n;
+    if constexpr ((n * n) % 4 == 0) {
+        // row-major flat index k = i·n + j, four at a time
+#pragma unroll
+        for (int k = 0; k < n * n; k += 4)
+            *reinterpret_cast<float4 *>(o + k) =
+                make_float4(m[k / n][k % n], m[(k + 1) / n][(k + 1) % n],
+                            m[(k + 2) / n][(k + 2) % n], m[(k + 3) / n][(k + 3) % n]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < n; ++i)
+#pragma unroll
+            for (int j = 0; j < n; ++j) o[i * n + j] = m[i][j];
     }
 }
 
@@ -100,6 +214,28 @@ __device__ __forceinline__ uint4 pre_mix8(const float (&h)[n], const uint4 (&xv)
 #pragma unroll
         for (int e = 0; e < 8; ++e) acc[e] = fmaf(h[i], t[e], acc[e]);
     }
+    return pack8(acc);
+}
+
+// §2.5 (2): row i of X_next for 8 channels, Σ_j H_res[i][j]·X[j] + H_post[i]·F_out,
+// fp32, rounded to bf16 (RNE).  hs: H_res row-major (n·n) followed by H_post (n).
+template <int n>
+__device__ __forceinline__ uint4 post_mix8(const float *hs, int i, const uint4 (&xv)[n],
+                                           const float (&f)[8])
+{
+    float acc[8], t[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < n; ++j) {
+        const float hij = hs[i * n + j];
+        unpack8(xv[j], t);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = fmaf(hij, t[e], acc[e]);
+    }
+    const float hq = hs[n * n + i];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = fmaf(hq, f[e], acc[e]);
     return pack8(acc);
 }
 

@@ -224,6 +224,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 
 // ------------------------------------------ programmatic dependent launch
 
+// Acquire load of a global 32-bit word at GPU scope: writes that another CTA
+// made before its release (or fenced atomic) on this word are visible after it.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Blocks until the grids this one depends on (the previous kernel in the
 // stream, when launched with programmatic stream serialisation) have
 // completed and their memory is visible.  A no-op otherwise.
@@ -234,6 +243,12 @@ __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;"
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ------------------------------------------------------ streaming access
+
+// Requests the line holding p into L2 without waiting for it or holding a register.
+__device__ __forceinline__ void prefetch_l2(const void *p)
+{
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {

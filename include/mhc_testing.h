@@ -49,6 +49,59 @@ int mhc_testing_forward_fused(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mh
                               mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
                               size_t workspace_bytes, mhc_stream_t stream);
 
+/*
+ * mhc_forward forced onto the four-kernel chain (mhc_gemm_rms, mhc_coeffs,
+ * mhc_pre_apply, mhc_post_res_apply), which mhc_forward itself takes only
+ * above its small-batch threshold.  Same arguments, rules and outputs as
+ * mhc_forward.
+ */
+int mhc_testing_forward_chain(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                              float alpha_pre, float alpha_post, float alpha_res,
+                              const float *bias, int iters, int64_t B, int n, int64_t C, float *Y,
+                              float *r, float *H_pre, float *H_post, float *H_res,
+                              mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
+                              size_t workspace_bytes, mhc_stream_t stream);
+
+/*
+ * mhc_forward forced onto the small-batch path: steps 1-4a in one cooperative
+ * launch (the split-K GEMM over all SMs, a bounded grid barrier, then each
+ * CTA's fixed-order reduction, coefficients and F_pre), then the X_next
+ * kernel.  mhc_forward takes this path by itself for B <= 128; this hook
+ * takes it for any B <= 512.  Same arguments, rules and outputs as
+ * mhc_forward; MHC_ERR_UNSUPPORTED for B > 512.
+ */
+int mhc_testing_forward_decode(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                               float alpha_pre, float alpha_post, float alpha_res,
+                               const float *bias, int iters, int64_t B, int n, int64_t C,
+                               float *Y, float *r, float *H_pre, float *H_post, float *H_res,
+                               mhc_bf16 *F_pre, mhc_bf16 *X_next, void *workspace,
+                               size_t workspace_bytes, mhc_stream_t stream);
+
+/*
+ * mhc_testing_forward_decode whose grid barrier waits for one arrival more
+ * than there are CTAs, so every CTA's wait runs out after `wait_limit_ns`
+ * nanoseconds of GPU time (clamped to [1 ms, 4 s]).  Each CTA then records
+ * MHC_ERR_TIMEOUT in the device status word (read with mhc_device_status)
+ * and returns without writing Y, r, H or F_pre; the X_next kernel still runs
+ * on whatever H_res and H_post hold.  The CUDA context stays usable.
+ */
+int mhc_testing_forward_decode_stalled(const mhc_bf16 *X, const mhc_bf16 *phi_t,
+                                       const mhc_bf16 *F_out, float alpha_pre, float alpha_post,
+                                       float alpha_res, const float *bias, int iters, int64_t B,
+                                       int n, int64_t C, float *Y, float *r, float *H_pre,
+                                       float *H_post, float *H_res, mhc_bf16 *F_pre,
+                                       mhc_bf16 *X_next, void *workspace, size_t workspace_bytes,
+                                       mhc_stream_t stream, uint64_t wait_limit_ns);
+
+/*
+ * out[i] = the reciprocal the Sinkhorn–Knopp normalisations and the sigmoids
+ * multiply by, of in[i]: the hardware's approximate reciprocal (rcp.approx,
+ * subnormal inputs and results flushed to zero).  `count` fp32 values, device
+ * pointers, 16-byte aligned, not overlapping.  MHC_ERR_INVALID for count < 0
+ * or a NULL pointer.
+ */
+int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -146,3 +146,24 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     res = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True,
                          text=True)
     assert res.returncode != 0 and "ImportError" in res.stderr
+
+
+def test_testing_hooks_validate_on_the_host():
+    assert L.mhc_testing_recip(A, B_, -1, None) == mhc.MHC_ERR_INVALID
+    assert L.mhc_testing_recip(A, B_, 0, None) == mhc.MHC_OK
+    assert L.mhc_testing_recip(None, B_, 4, None) == mhc.MHC_ERR_INVALID
+    assert L.mhc_testing_recip(A + 4, B_, 4, None) == mhc.MHC_ERR_ALIGN
+    assert L.mhc_testing_recip(A, A + 8, 4, None) in (mhc.MHC_ERR_ALIGN, mhc.MHC_ERR_INVALID)
+    assert L.mhc_testing_recip(A, B_, 4, None) == NO_DEVICE
+    for name in ("mhc_testing_forward_chain", "mhc_testing_forward_decode"):
+        f = getattr(L, name)
+        args = [A, B_, C_, 0.01, 0.01, 0.01, D, 20, 4, 4, 256, E, F, G, H, I, J,
+                0x1_0000_0000, W, 1 << 30, None]
+        assert f(*args) == NO_DEVICE
+        args[8] = 0
+        assert f(*args) == mhc.MHC_OK  # empty batch
+        args[8], args[9] = 4, 9
+        assert f(*args) == mhc.MHC_ERR_UNSUPPORTED
+    args = [A, B_, C_, 0.01, 0.01, 0.01, D, -1, 4, 4, 256, E, F, G, H, I, J, 0x1_0000_0000, W,
+            1 << 30, None, 50_000_000]
+    assert L.mhc_testing_forward_decode_stalled(*args) == mhc.MHC_ERR_INVALID

@@ -1,15 +1,18 @@
-"""Failure detection on the GPU without a fault: a wait inside the GEMM+RMS
-kernel is made to run out (one pipeline stage is left unfilled through the
-test hook of include/mhc_testing.h, with a 50 ms wait limit).  The kernel must
-report MHC_ERR_TIMEOUT through the device status word, return cleanly, and
-leave the CUDA context usable for the next call.
+"""Failure detection on the GPU without a fault: a wait inside a kernel is
+made to run out through the test hooks of include/mhc_testing.h, with a 50 ms
+wait limit: one pipeline stage of the GEMM+RMS kernel left unfilled, or the
+grid barrier of the small-batch forward kernel waiting for one CTA more than
+the grid has.  The kernel must report MHC_ERR_TIMEOUT through the device
+status word, return cleanly, and leave the CUDA context usable for the next
+call.
 """
 import numpy as np
 import pytest
 import torch
 
 import oracle
-from gpu_util import R_REL, assert_rel, assert_Y_close, cuda_ok, dev_bf16, host64, phi_KN
+from gpu_util import (H_TOL, R_REL, assert_abs, assert_bf16_close, assert_rel, assert_Y_close,
+                      cuda_ok, dev_bf16, dev_f32, host64, phi_KN)
 from synth import WORKLOADS, make_inputs
 
 pytestmark = [pytest.mark.gpu,
@@ -61,4 +64,39 @@ def test_hook_without_stall_is_the_normal_call():
     a = _gemm(X, phi_t, wl, stall_stage=-1, limit_ns=4_000_000_000)
     b = _gemm(X, phi_t, wl)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+
+
+def _forward(inp, wl, stalled=False):
+    X = dev_bf16(inp["X"])
+    out = {k: v.zero_() for k, v in mhc.alloc_outputs(wl.B, wl.n, wl.C).items()}
+    args = (X, dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), wl.alpha_pre, wl.alpha_post,
+            wl.alpha_res, dev_f32(inp["bias"]), wl.iters, wl.B, wl.n, wl.C, out["Y"], out["r"],
+            out["H_pre"], out["H_post"], out["H_res"], out["F_pre"], out["X_next"], out["ws"])
+    if stalled:
+        mhc.mhc_testing_forward_decode_stalled(*args, 50_000_000)
+    else:
+        mhc.mhc_testing_forward_decode(*args)
+    torch.cuda.synchronize()  # a fault would raise here
+    return out
+
+
+def test_stalled_grid_barrier_reports_timeout_and_context_survives():
+    wl = WORKLOADS["decode32"]
+    inp = make_inputs(wl, seed=11)
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+    out = _forward(inp, wl, stalled=True)
+    assert mhc.mhc_device_status() == mhc.MHC_ERR_TIMEOUT
+    # no CTA passed the barrier, so nothing of steps 1-4a was written
+    for k in ("Y", "r", "H_pre", "H_post", "H_res"):
+        assert not bool(out[k].any()), k
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+    out = _forward(inp, wl)
+    ref = oracle.forward(inp["X"], phi_KN(inp["phi_t"]), inp["F_out"], wl.n, wl.C, wl.alpha_pre,
+                         wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters)
+    assert_Y_close(host64(out["Y"]), ref["Y"], inp["X"], inp["phi_t"])
+    assert_rel(host64(out["r"]), ref["r"], R_REL, "r")
+    assert_abs(host64(out["H_res"]), ref["H_res"], H_TOL, "H_res")
+    assert_bf16_close(host64(out["F_pre"]), ref["F_pre"], "F_pre")
+    assert_bf16_close(host64(out["X_next"]), ref["X_next"], "X_next")
     assert mhc.mhc_device_status() == mhc.MHC_OK

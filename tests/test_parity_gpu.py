@@ -201,7 +201,12 @@ def test_post_res_apply_permutation_is_exact():
 # ------------------------------------------------------------ forward
 
 
-def forward_gpu(inp, wl, inplace=False, fused=False):
+FORWARD_PATHS = {"fused": "mhc_testing_forward_fused", "chain": "mhc_testing_forward_chain",
+                 "decode": "mhc_testing_forward_decode"}
+
+
+def forward_gpu(inp, wl, inplace=False, path="auto"):
+    """mhc_forward ("auto": the library picks the path) or one forced path."""
     X = dev_bf16(inp["X"])
     B = X.shape[0]
     out = mhc.alloc_outputs(B, wl.n, wl.C)
@@ -209,12 +214,12 @@ def forward_gpu(inp, wl, inplace=False, fused=False):
         out["X_next"] = X
     args = (X, dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), wl.alpha_pre, wl.alpha_post,
             wl.alpha_res, dev_f32(inp["bias"]), wl.iters)
-    if fused:
-        mhc.mhc_testing_forward_fused(*args, B, wl.n, wl.C, out["Y"], out["r"], out["H_pre"],
-                                      out["H_post"], out["H_res"], out["F_pre"], out["X_next"],
-                                      out["ws"])
-    else:
+    if path == "auto":
         mhc.forward(*args, wl.n, wl.C, out=out)
+    else:
+        getattr(mhc, FORWARD_PATHS[path])(*args, B, wl.n, wl.C, out["Y"], out["r"],
+                                          out["H_pre"], out["H_post"], out["H_res"],
+                                          out["F_pre"], out["X_next"], out["ws"])
     torch.cuda.synchronize()
     return out
 
@@ -288,10 +293,10 @@ FUSED_SHAPES = [(1000, 4, 7168), (1100, 4, 4096), (600, 8, 2048), (256, 4, 2048)
 def test_forward_fused_path_shapes(B, n, C):
     wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
     inp = make_inputs(wl, seed=6)
-    out = forward_gpu(inp, wl, fused=True)
+    out = forward_gpu(inp, wl, path="fused")
     check_forward(out, inp, wl)
     check_properties(out, wl)
-    again = forward_gpu(inp, wl, fused=True)
+    again = forward_gpu(inp, wl, path="fused")
     for k in ("Y", "r", "H_res", "F_pre", "X_next"):
         assert torch.equal(out[k], again[k]), k  # fixed-order sums: bitwise reproducible
 
@@ -300,45 +305,98 @@ def test_forward_fused_path_rejects_one_tile():
     wl = WORKLOADS["tiny"]
     inp = make_inputs(wl, seed=6)
     with pytest.raises(mhc.MhcError) as ei:
-        forward_gpu(inp, wl, fused=True)
+        forward_gpu(inp, wl, path="fused")
     assert ei.value.status == mhc.MHC_ERR_UNSUPPORTED
 
 
 @pytest.mark.parametrize("B,n,C", ODD_SHAPES)
-def test_forward_odd_shapes(B, n, C):
+@pytest.mark.parametrize("path", ["auto", "chain"])
+def test_forward_odd_shapes(B, n, C, path):
     wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
     inp = make_inputs(wl, seed=3)
-    check_forward(forward_gpu(inp, wl), inp, wl)
+    check_forward(forward_gpu(inp, wl, path=path), inp, wl)
 
 
-def test_forward_in_place():
-    wl = WORKLOADS["tiny"]
+@pytest.mark.parametrize("name", ["tiny", "decode1", "decode128"])
+def test_forward_chain_path_small_batches(name):
+    """mhc_forward takes the one-launch path for these; the chain must agree with the oracle too."""
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, seed=0)
+    out = forward_gpu(inp, wl, path="chain")
+    check_forward(out, inp, wl)
+    check_properties(out, wl)
+
+
+# shapes for the small-batch one-launch path: every n, ragged K blocks, ragged
+# and several token tiles (up to its 512-token limit), one CTA and all SMs
+DECODE_SHAPES = ODD_SHAPES + [(1, 4, 7168), (1, 8, 7168), (128, 4, 7168), (129, 4, 7168),
+                              (300, 8, 512), (512, 4, 7168), (77, 6, 1000)]
+
+
+@pytest.mark.parametrize("B,n,C", DECODE_SHAPES)
+def test_forward_decode_path_shapes(B, n, C):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=8)
+    out = forward_gpu(inp, wl, path="decode")
+    check_forward(out, inp, wl)
+    check_properties(out, wl)
+    again = forward_gpu(inp, wl, path="decode")
+    for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre", "X_next"):
+        assert torch.equal(out[k], again[k]), k  # fixed-order sums: bitwise reproducible
+
+
+def test_forward_decode_path_f_pre_uses_the_written_h_pre():
+    """Every CTA that mixes a token's channels must form the same H_pre bits as the
+    CTA that stores it.  With X one-hot over the streams (channel c lives in
+    stream c mod n only), F_pre[c] is the bf16 rounding of the fp32 product
+    H_pre[c mod n]·x[c], bit for bit, so a CTA that used other bits would show."""
+    B, n, C = 3, 4, 7168  # each token's channels are spread over ~50 CTAs
+    wl = WORKLOADS["decode1"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=9)
+    x = inp["X"].reshape(B, n, C)
+    keep = (np.arange(C)[None, :] % n) == np.arange(n)[:, None]  # [n][C]
+    inp["X"] = np.where(keep[None], x, np.uint16(0)).reshape(B, n * C).astype(np.uint16)
+    out = forward_gpu(inp, wl, path="decode")
+    Hp = host64(out["H_pre"])  # exact fp32 values
+    xs = f64(inp["X"]).reshape(B, n, C)[:, np.arange(C) % n, np.arange(C)]
+    prod32 = (Hp[:, np.arange(C) % n] * xs).astype(np.float32)  # exact product, one rounding
+    want = synth.f32_to_bf16_bits(prod32)
+    assert np.array_equal(host_bits(out["F_pre"]), want)
+
+
+@pytest.mark.parametrize("path", ["auto", "decode"])
+def test_forward_decode_in_place(path):
+    wl = WORKLOADS["decode32"]
     inp = make_inputs(wl, seed=4)
-    ref_out = forward_gpu(inp, wl)
-    out = forward_gpu(inp, wl, inplace=True)
+    ref_out = forward_gpu(inp, wl, path=path)
+    out = forward_gpu(inp, wl, inplace=True, path=path)
     assert torch.equal(out["X_next"], ref_out["X_next"])
     check_forward(out, inp, wl)
 
 
-def test_forward_empty_batch_is_a_noop():
-    wl = WORKLOADS["tiny"]
-    e = torch.empty(0, wl.n * wl.C, dtype=torch.bfloat16, device="cuda")
-    phi = torch.zeros(wl.N, wl.K, dtype=torch.bfloat16, device="cuda")
-    out = mhc.alloc_outputs(0, wl.n, wl.C)
-    mhc.forward(e, phi, torch.empty(0, wl.C, dtype=torch.bfloat16, device="cuda"), 0.01, 0.01,
-                0.01, torch.zeros(wl.N, device="cuda"), 20, wl.n, wl.C, out=out)
-
-
-def test_workspace_too_small_is_rejected():
-    wl = WORKLOADS["tiny"]
-    inp = make_inputs(wl, seed=0)
-    out = mhc.alloc_outputs(wl.B, wl.n, wl.C)
-    out["ws"] = out["ws"][:16]
+def test_forward_decode_path_rejects_large_batches():
+    wl = WORKLOADS["tiny"].with_(B=513)
+    inp = make_inputs(wl, seed=6)
     with pytest.raises(mhc.MhcError) as ei:
-        mhc.forward(dev_bf16(inp["X"]), dev_bf16(inp["phi_t"]), dev_bf16(inp["F_out"]), 0.01,
-                    0.01, 0.01, dev_f32(inp["bias"]), 20, wl.n, wl.C, out=out)
-    assert ei.value.status == mhc.MHC_ERR_WORKSPACE
+        forward_gpu(inp, wl, path="decode")
+    assert ei.value.status == mhc.MHC_ERR_UNSUPPORTED
 
 
-def test_device_status_is_clean():
-    assert mhc.mhc_device_status() == mhc.MHC_OK
+def test_sinkhorn_reciprocal_within_one_ulp():
+    """The reciprocal of the Sinkhorn steps and the sigmoids (the hardware's
+    approximate one): within one ulp of 1/x (fp64) wherever x and 1/x are normal
+    fp32 numbers, both signs; the row and column sums it sees lie in [1, 8]."""
+    rng = np.random.default_rng(5)
+    mags = 10.0 ** rng.uniform(-37, 37, 200000)
+    x = np.concatenate([mags * rng.choice([-1.0, 1.0], mags.size),
+                        rng.uniform(1.0, 8.0, 100000),
+                        2.0 ** np.arange(-120, 121)]).astype(np.float32)
+    xd = torch.from_numpy(x).cuda()
+    out = torch.empty_like(xd)
+    mhc.mhc_testing_recip(xd, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    exact = 1.0 / x.astype(np.float64)
+    ulp = np.spacing(np.abs(exact).astype(np.float32)).astype(np.float64)
+    err = np.abs(got - exact) / ulp
+    assert float(err.max()) <= 1.0, float(err.max())
