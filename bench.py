@@ -8,8 +8,10 @@ so no L2 flush is needed between steps.
 
 Reported:
   value        tokens/s over all ranks (weak scaling: every rank runs its own batch)
-  e2e          the same metric through the public API with pinned host buffers:
-               H2D of the step's inputs, the forward, D2H of its outputs, all timed
+  e2e          the same metric through the public C-ABI call over host buffers
+               (mhc_forward_host, pinned memory): H2D of the step's inputs X and
+               F_out, the forward, D2H of every output, all timed (the call
+               overlaps them chunk by chunk; the weights stay on the device)
   roofline     the dominant kernel's algorithmic bytes / its CUDA-event time,
                against the measured HBM copy bandwidth (MEASURED_PEAKS.json)
   cpu_baseline the fp64 oracle on the host cores, on a bounded token sample
@@ -323,6 +325,27 @@ def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out
             for i, k in enumerate(KERNELS)}
 
 
+def host_link_copy(h_X, h_F, h_out, X, F_out, out, stream):
+    """One step's bytes over the host link with nothing else running: X and
+    F_out host->device on `stream` while every output goes device->host on a
+    second stream; returns the function that enqueues it."""
+    import torch
+
+    side = torch.cuda.Stream(device=X.device)
+
+    def once():
+        side.wait_stream(stream)
+        with torch.cuda.stream(stream):
+            X.copy_(h_X, non_blocking=True)
+            F_out.copy_(h_F, non_blocking=True)
+        with torch.cuda.stream(side):
+            for k, v in h_out.items():
+                v.copy_(out[k], non_blocking=True)
+        stream.wait_stream(side)
+
+    return once
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,6 +365,8 @@ def main() -> int:
                          "forced through its test hook: chain (four kernels), decode (the "
                          "small-batch one-launch steps 1-4a), fused (the large-batch one-kernel "
                          "steps 1-4a)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="latency mode: the workload with this many tokens instead")
     ap.add_argument("--mode", default="full", choices=["full", "kernels", "latency"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
                          "latency: microseconds per mhc_forward (stream and CUDA graph)")
@@ -352,6 +377,10 @@ def main() -> int:
     import synth
 
     wl = synth.WORKLOADS[args.workload]
+    if args.tokens is not None:
+        if args.mode != "latency":
+            ap.error("--tokens only applies to --mode latency")
+        wl = wl.with_(name="%s_B%d" % (wl.name, args.tokens), B=args.tokens)
     if args.impl == "reference":
         return run_reference(args, wl)
 
@@ -471,43 +500,44 @@ def main() -> int:
                         "frac": algo[k] / (per_kernel_ms[k] / 1e3) / 1e9 / peak}
                     for k in KERNELS}
 
-    # ---- end to end through the public API with pinned host buffers
+    # ---- end to end through the public API with pinned host buffers: the
+    # host-buffer forward copies each step's inputs (X, F_out) to the device and
+    # every output back, overlapped with the compute chunk by chunk; the
+    # weights (phi_t, b) stay resident on the device as in a model
     h_X = torch.empty(X.shape, dtype=X.dtype, pin_memory=True)
     h_X.copy_(X)
     h_F = torch.empty(F_out.shape, dtype=F_out.dtype, pin_memory=True)
     h_F.copy_(F_out)
-    h_phi = phi_t.cpu().pin_memory()
-    h_bias = bias.cpu().pin_memory()
-    h_out = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True)
-             for k, v in out.items() if k != "ws"}
-    d_in = {"X": torch.empty_like(X), "F": torch.empty_like(F_out),
-            "phi": torch.empty_like(phi_t), "bias": torch.empty_like(bias)}
+    h_out = mhc.alloc_host_outputs(B, n, C, pin=True)
+    scratch = mhc.host_scratch(B, n, C, dev)
 
     def e2e_step():
-        d_in["X"].copy_(h_X, non_blocking=True)
-        d_in["F"].copy_(h_F, non_blocking=True)
-        d_in["phi"].copy_(h_phi, non_blocking=True)
-        d_in["bias"].copy_(h_bias, non_blocking=True)
-        mhc.mhc_forward(d_in["X"], d_in["phi"], d_in["F"], wl.alpha_pre, wl.alpha_post,
-                        wl.alpha_res, d_in["bias"], wl.iters, B, n, C, out["Y"], out["r"],
-                        out["H_pre"], out["H_post"], out["H_res"], out["F_pre"], out["X_next"],
-                        out["ws"], stream)
-        for k, v in h_out.items():
-            v.copy_(out[k], non_blocking=True)
+        mhc.mhc_forward_host(h_X, phi_t, h_F, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                             wl.iters, B, n, C, h_out["Y"], h_out["r"], h_out["H_pre"],
+                             h_out["H_post"], h_out["H_res"], h_out["F_pre"], h_out["X_next"],
+                             scratch, stream)
 
-    h2d = sum(t.numel() * t.element_size() for t in (h_X, h_F, h_phi, h_bias))
+    h2d = sum(t.numel() * t.element_size() for t in (h_X, h_F))
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    link_once = host_link_copy(h_X, h_F, h_out, X, F_out, out, stream)
     for _ in range(2):
         e2e_step()
+        link_once()
     barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
+    # the e2e steps and, after each, the same bytes as plain copies (the host
+    # link's own bound; the link is shared with the node's other work, so the
+    # two are interleaved rather than taken one after the other)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.e2e_steps)]
+    for e in ev:
+        e[0].record(stream)
         e2e_step()
-    e1.record(stream)
+        e[1].record(stream)
+        link_once()
+        e[2].record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev) / args.e2e_steps
+    e2e_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev), dist, dev) / args.e2e_steps
     e2e_value = tokens_per_second(B, world, 1, e2e_ms)
+    link_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / args.e2e_steps
 
     # ---- CPU baseline: the fp64 oracle on the host cores (rank 0 only)
     cpu = None
@@ -538,7 +568,9 @@ def main() -> int:
                      "algorithmic_bytes": algo[dom], "peak_source": peak_src},
         "kernels": kernels_json,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "link_copy_ms_per_step": link_ms,
+                "link_frac": link_ms / e2e_ms if e2e_ms > 0 else None},
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,

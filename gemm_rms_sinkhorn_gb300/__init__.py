@@ -46,6 +46,9 @@ _SIGS = {
     "mhc_forward": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
+    "mhc_forward_host_scratch_bytes": ([_i64, _i32, _i64], _sz),
+    "mhc_forward_host": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_gemm_rms_noalloc": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp], _i32),
     # test hook (include/mhc_testing.h), not part of the stable API
     "mhc_testing_gemm_rms_stalled": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _i64,
@@ -95,6 +98,19 @@ def _ptr(t, dtype, name):
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def _hptr(t, dtype, name):
+    """Host pointer of a contiguous CPU tensor of `dtype`."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.is_cuda:
+        raise ValueError("%s must be a host (CPU) tensor" % name)
     if not t.is_contiguous():
         raise ValueError("%s must be contiguous" % name)
     return t.data_ptr()
@@ -192,7 +208,7 @@ def mhc_testing_forward_chain(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res,
 def mhc_testing_forward_decode(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters,
                                B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws,
                                stream=None):
-    """Test hook: mhc_forward through the small-batch one-launch path (B <= 512)."""
+    """Test hook: mhc_forward through the small-batch one-launch path (B <= 4096)."""
     _forward_like("mhc_testing_forward_decode", X, phi_t, F_out, alpha_pre, alpha_post,
                   alpha_res, bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws,
                   stream)
@@ -212,6 +228,38 @@ def mhc_testing_recip(x, out, stream=None):
     f = torch.float32
     _check(_lib.mhc_testing_recip(_ptr(x, f, "x"), _ptr(out, f, "out"), x.numel(),
                                   _stream(stream)), "mhc_testing_recip")
+
+
+def mhc_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                     Y, r, H_pre, H_post, H_res, F_pre, X_next, scratch, stream=None):
+    """mhc_forward over host tensors (X, F_out in; Y ... X_next out; page-locked for
+    overlap) with device-resident phi_t and bias and a device ``scratch`` of
+    ``host_scratch(B, n, C)``.  Stream-ordered: synchronise before reading outputs."""
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(scratch)
+    _check(_lib.mhc_forward_host(
+        _hptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), _hptr(F_out, bf, "F_out"), alpha_pre,
+        alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n, C, _hptr(Y, f, "Y"),
+        _hptr(r, f, "r"), _hptr(H_pre, f, "H_pre"), _hptr(H_post, f, "H_post"),
+        _hptr(H_res, f, "H_res"), _hptr(F_pre, bf, "F_pre"), _hptr(X_next, bf, "X_next"), p,
+        nb, _stream(stream)), "mhc_forward_host")
+
+
+def host_scratch(B: int, n: int, C: int, device=None) -> "torch.Tensor":
+    """Device scratch of ``mhc_forward_host`` for (B, n, C)."""
+    nbytes = _lib.mhc_forward_host_scratch_bytes(B, n, C)
+    if nbytes == 0 and B > 0:
+        raise MhcError(MHC_ERR_INVALID, "mhc_forward_host_scratch_bytes")
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device or "cuda")
+
+
+def alloc_host_outputs(B: int, n: int, C: int, pin: bool = True) -> dict:
+    """Host output buffers of ``mhc_forward_host`` (page-locked when ``pin``)."""
+    N = n * n + 2 * n
+    f, bf = torch.float32, torch.bfloat16
+    mk = lambda *shape, dtype=f: torch.empty(*shape, dtype=dtype, pin_memory=pin)
+    return dict(Y=mk(B, N), r=mk(B), H_pre=mk(B, n), H_post=mk(B, n), H_res=mk(B, n, n),
+                F_pre=mk(B, C, dtype=bf), X_next=mk(B, n * C, dtype=bf))
 
 
 def mhc_gemm_rms_noalloc(X, phi_t, B, n, C, Y, r, stream=None):

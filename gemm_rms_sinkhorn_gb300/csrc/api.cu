@@ -103,6 +103,23 @@ int check_overlap(const Buf *outs, int n_out, const Buf *ins, int n_in, const vo
     return MHC_OK;
 }
 
+// Where each pointer lives: host memory (page-locked or pageable) or device
+// memory, as the runtime records it.  MHC_ERR_INVALID on a mismatch.
+int check_memory_kind(const Buf *bufs, int count, bool host)
+{
+    for (int i = 0; i < count; ++i) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, bufs[i].p) != cudaSuccess) {
+            cudaGetLastError();  // not sticky; clear it
+            return MHC_ERR_INVALID;
+        }
+        const bool is_host = a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
+        const bool is_dev = a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+        if (host ? !is_host : !is_dev) return MHC_ERR_INVALID;
+    }
+    return MHC_OK;
+}
+
 int check_device(DeviceInfo *info)
 {
     if (current_device_info(info) != cudaSuccess) return MHC_ERR_CUDA;
@@ -113,8 +130,30 @@ int check_device(DeviceInfo *info)
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MHC_OK : MHC_ERR_CUDA; }
 
 size_t bf16_bytes(int64_t count) { return static_cast<size_t>(count) * 2; }
+size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 
-// Workspace of every forward path (and of mhc_gemm_rms), whichever is largest.
+#define MHC_TRY(expr)                   \
+    do {                                \
+        const int st_ = (expr);         \
+        if (st_ != MHC_OK) return st_;  \
+    } while (0)
+
+// Batches up to this size take the one-launch steps 1-4a kernel.  Measured on
+// GB300 against the four-kernel chain: about 2x faster up to 512 tokens (the
+// chain is bound by launch and reduction latency there), 10-45% faster at
+// 1024-2048, 4-7% at 3072, even at 4096 (n = 4 and 8, C = 256..7168).
+constexpr int64_t kDecodeMaxTokens = 3072;
+
+enum class Path {
+    Auto,           // decode_pre for small batches, else the four-kernel chain
+    Chain,          // gemm_rms, coeffs, pre_apply
+    Fused,          // fused_pre (test hook)
+    Decode,         // decode_pre (test hook for any eligible batch)
+    DecodeStalled,  // decode_pre whose grid barrier never completes (test hook)
+};
+
+}  // namespace
+
 size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
 {
     size_t w = gemm_rms_workspace_bytes(B, n, C, num_sms);
@@ -125,26 +164,49 @@ size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
     return w;
 }
 
-// Batches up to this size take the one-launch steps 1-4a kernel: there the
-// forward is bound by launch and reduction latency, not by HBM.
-constexpr int64_t kDecodeMaxTokens = 128;
+// The kernels of one forward for a path (arguments already valid and the path
+// eligible): steps 1-4a by the path, then the X_next kernel.
+static cudaError_t launch_forward(const uint16_t *X, const uint16_t *phi_t, const uint16_t *F_out,
+                                  float a_pre, float a_post, float a_res, const float *bias,
+                                  int iters, int64_t B, int n, int64_t C, float *Y, float *r,
+                                  float *H_pre, float *H_post, float *H_res, uint16_t *F_pre,
+                                  uint16_t *X_next, void *workspace, int num_sms, cudaStream_t s,
+                                  Path path, uint64_t wait_limit_ns)
+{
+    if (path == Path::Auto)
+        path = B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C) ? Path::Decode : Path::Chain;
+    cudaError_t e;
+    if (path == Path::Fused) {
+        // steps 1-4a in one kernel that reads X from HBM once
+        e = launch_fused_pre(X, phi_t, a_pre, a_post, a_res, bias, iters, B, n, C, Y, r, H_pre,
+                             H_post, H_res, F_pre, workspace, num_sms, s);
+    } else if (path == Path::Decode || path == Path::DecodeStalled) {
+        e = launch_decode_pre(X, phi_t, a_pre, a_post, a_res, bias, iters, B, n, C, Y, r, H_pre,
+                              H_post, H_res, F_pre, workspace, num_sms, s, wait_limit_ns,
+                              path == Path::DecodeStalled ? 1 : 0);
+    } else {
+        e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, num_sms, s);
+        if (e == cudaSuccess)
+            e = launch_coeffs(Y, r, a_pre, a_post, a_res, bias, iters, B, n, H_pre, H_post,
+                              H_res, s);
+        if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    }
+    if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
+    return e;
+}
 
-enum class Path {
-    Auto,           // decode_pre for small batches, else the four-kernel chain
-    Chain,          // gemm_rms, coeffs, pre_apply
-    Fused,          // fused_pre (test hook)
-    Decode,         // decode_pre (test hook for any eligible batch)
-    DecodeStalled,  // decode_pre whose grid barrier never completes (test hook)
-};
-size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
+cudaError_t run_forward_device(const uint16_t *X, const uint16_t *phi_t, const uint16_t *F_out,
+                               float a_pre, float a_post, float a_res, const float *bias,
+                               int iters, int64_t B, int n, int64_t C, float *Y, float *r,
+                               float *H_pre, float *H_post, float *H_res, uint16_t *F_pre,
+                               uint16_t *X_next, void *workspace, int num_sms,
+                               cudaStream_t stream)
+{
+    return launch_forward(X, phi_t, F_out, a_pre, a_post, a_res, bias, iters, B, n, C, Y, r,
+                          H_pre, H_post, H_res, F_pre, X_next, workspace, num_sms, stream,
+                          Path::Auto, kWaitLimitNs);
+}
 
-#define MHC_TRY(expr)                   \
-    do {                                \
-        const int st_ = (expr);         \
-        if (st_ != MHC_OK) return st_;  \
-    } while (0)
-
-}  // namespace
 }  // namespace mhc
 
 using namespace mhc;
@@ -177,29 +239,15 @@ static int forward_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_b
     outs[7].bytes = need;
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e;
-    if (path == Path::Auto)
-        path = B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C) ? Path::Decode : Path::Chain;
-    if (path == Path::Fused) {
-        if (!fused_pre_eligible(B, n, C, info.num_sms)) return MHC_ERR_UNSUPPORTED;
-        // steps 1-4a in one kernel that reads X from HBM once
-        e = launch_fused_pre(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y,
-                             r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s);
-    } else if (path == Path::Decode || path == Path::DecodeStalled) {
-        if (!decode_pre_eligible(B, n, C)) return MHC_ERR_UNSUPPORTED;
-        e = launch_decode_pre(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y,
-                              r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
-                              wait_limit_ns, path == Path::DecodeStalled ? 1 : 0);
-    } else {
-        e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
-        if (e == cudaSuccess)
-            e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
-                              H_post, H_res, s);
-        if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
-    }
-    if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
-    return cuda_status(e);
+    if (path == Path::Fused && !fused_pre_eligible(B, n, C, info.num_sms))
+        return MHC_ERR_UNSUPPORTED;
+    if ((path == Path::Decode || path == Path::DecodeStalled) && !decode_pre_eligible(B, n, C))
+        return MHC_ERR_UNSUPPORTED;
+    return cuda_status(launch_forward(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias,
+                                      iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next,
+                                      workspace, info.num_sms,
+                                      reinterpret_cast<cudaStream_t>(stream), path,
+                                      wait_limit_ns));
 }
 
 static int gemm_rms_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int64_t C,
@@ -383,6 +431,48 @@ int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t s
     DeviceInfo info;
     MHC_TRY(check_device(&info));
     return cuda_status(launch_recip(in, out, count, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t mhc_forward_host_scratch_bytes(int64_t B, int n, int64_t C)
+{
+    if (check_shape(B, n, C, true) != MHC_OK || B == 0) return 0;
+    DeviceInfo info;
+    if (current_device_info(&info) != cudaSuccess) return 0;
+    return host_chunk_layout(B, n, C, info.num_sms).total;
+}
+
+int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                     void *scratch, size_t scratch_bytes, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf host_in[] = {{X, bf16_bytes(B * K)}, {F_out, bf16_bytes(B * C)}};
+    const Buf dev_in[] = {{phi_t, bf16_bytes(int64_t{N} * K)}, {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {F_pre, bf16_bytes(B * C)},
+                  {X_next, bf16_bytes(B * K)},   {scratch, scratch_bytes}};
+    const Buf ins[] = {host_in[0], host_in[1], dev_in[0], dev_in[1]};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 8));
+    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    MHC_TRY(check_memory_kind(host_in, 2, true));
+    MHC_TRY(check_memory_kind(outs, 7, true));
+    MHC_TRY(check_memory_kind(dev_in, 2, false));
+    MHC_TRY(check_memory_kind(outs + 7, 1, false));
+    if (scratch_bytes < host_chunk_layout(B, n, C, info.num_sms).total) return MHC_ERR_WORKSPACE;
+    return cuda_status(run_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias,
+                                        iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre,
+                                        X_next, scratch, info.num_sms,
+                                        reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int mhc_device_status(int *status)

@@ -43,7 +43,7 @@ using pipe::SegIter;
 
 constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
 constexpr int kRingBudget = 160 * 1024;
-constexpr int kMaxTokens = 512;   // largest batch this path takes
+constexpr int kMaxTokens = 4096;  // largest batch this path takes
 constexpr int kSegLen = 32;       // contributors per first-level segment of the sum
 constexpr int kRedFloats = 16384; // first-level segment sums of one token batch
 constexpr int kTokBatch = 32;     // tokens whose coefficients are formed together
@@ -267,22 +267,35 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                 if (t * C8 >= lo) store_token_coeffs<n>(t, hp, hq, mres, H_pre, H_post, H_res);
             }
         } else {
-            // F_pre of this CTA's items of these tokens, token by token
+            // F_pre of this CTA's items of these tokens, token by token, kU
+            // items a thread at a time so that their loads are in flight together
             constexpr int kMixThreads = kThreads - 32;
+            constexpr int kU = n <= 4 ? 4 : (n <= 6 ? 2 : 1);
             for (int j = 0; j < cnt; ++j) {
                 const int64_t t = t0 + j;
-                const int64_t a = t * C8 > lo ? t * C8 : lo;
-                const int64_t b = (t + 1) * C8 < hi ? (t + 1) * C8 : hi;
+                const int64_t a = (t * C8 > lo ? t * C8 : lo) - t * C8;
+                const int64_t b = ((t + 1) * C8 < hi ? (t + 1) * C8 : hi) - t * C8;
                 float h[n];
 #pragma unroll
                 for (int i = 0; i < n; ++i) h[i] = hps[j * n + i];
-                for (int64_t c8 = a - t * C8 + threadIdx.x; c8 < b - t * C8; c8 += kMixThreads) {
-                    const uint16_t *x = X + t * n * C + c8 * 8;
-                    uint4 xv[n];
+                const uint16_t *xt = X + t * n * C;
+                uint16_t *ft = F_pre + t * C;
+                for (int64_t c0 = a + threadIdx.x; c0 < b; c0 += kMixThreads * kU) {
+                    uint4 xv[kU][n];
 #pragma unroll
-                    for (int i = 0; i < n; ++i)
-                        xv[i] = __ldg(reinterpret_cast<const uint4 *>(x + i * C));
-                    ptx::st_stream_v4(F_pre + t * C + c8 * 8, pre_mix8<n>(h, xv));
+                    for (int u = 0; u < kU; ++u) {
+                        const int64_t c8 = c0 + u * kMixThreads;
+                        if (c8 < b) {
+#pragma unroll
+                            for (int i = 0; i < n; ++i)
+                                xv[u][i] = __ldg(reinterpret_cast<const uint4 *>(xt + i * C + c8 * 8));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int64_t c8 = c0 + u * kMixThreads;
+                        if (c8 < b) ptx::st_stream_v4(ft + c8 * 8, pre_mix8<n>(h, xv[u]));
+                    }
                 }
             }
         }

@@ -103,6 +103,38 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
                               int barrier_extra = 0);
 cudaError_t read_and_clear_decode_status(int *status);
 
+// ---- the whole forward on device buffers (api.cu), arguments already valid
+// Workspace of every forward path (and of mhc_gemm_rms), whichever is largest.
+size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+// mhc_forward's own choice of path: the one-launch steps 1-4a kernel for small
+// batches, else the four-kernel chain; then the X_next kernel.
+cudaError_t run_forward_device(const uint16_t *X, const uint16_t *phi_t, const uint16_t *F_out,
+                               float a_pre, float a_post, float a_res, const float *bias,
+                               int iters, int64_t B, int n, int64_t C, float *Y, float *r,
+                               float *H_pre, float *H_post, float *H_res, uint16_t *F_pre,
+                               uint16_t *X_next, void *workspace, int num_sms,
+                               cudaStream_t stream);
+
+// ---- the forward over host buffers (host_pipeline.cu)
+// Tokens a chunk carries through the device: small enough that the first
+// copy in and the last copy out, which nothing overlaps, stay short, large
+// enough that each copy runs at link speed.
+constexpr int64_t kHostChunkTokens = 1024;
+constexpr int kHostSlots = 3;               // chunks in flight (copy in, compute, copy out)
+// Byte sizes (each 256-byte aligned) of one chunk slot's bf16 buffers (x,
+// f_out, f_pre), of the batch-wide fp32 outputs (y, r, h_*), of the forward
+// workspace shared by the chunks, and of the whole scratch.
+struct HostChunkLayout {
+    int64_t chunk_tokens;
+    size_t x, f_out, f_pre, y, r, h_pre, h_post, h_res, slot, workspace, total;
+};
+HostChunkLayout host_chunk_layout(int64_t B, int n, int64_t C, int num_sms);
+cudaError_t run_forward_host(const uint16_t *X, const uint16_t *phi_t, const uint16_t *F_out,
+                             float a_pre, float a_post, float a_res, const float *bias, int iters,
+                             int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                             float *H_post, float *H_res, uint16_t *F_pre, uint16_t *X_next,
+                             void *scratch, int num_sms, cudaStream_t stream);
+
 // ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
 cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,
                           const float *bias, int iters, int64_t B, int n, float *H_pre,

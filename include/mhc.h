@@ -12,7 +12,9 @@
  *                       H_post = 2σ(H̃_post), H_res = Sinkhorn(H̃_res) (§2.3, §2.4, §3.2, §3.3)
  *   mhc_pre_apply       F_pre = Σ_i H_pre[i]·X[i]                 (§2.5)
  *   mhc_post_res_apply  X_next[i] = Σ_j H_res[i][j]·X[j] + H_post[i]·F_out (§2.5, §3.4)
- *   mhc_forward         the four calls above, in order, on one stream
+ *   mhc_forward         steps 1-4b on one stream (the four calls above, or for
+ *                       B <= 3072 steps 1-4a in one launch, then step 4b)
+ *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
  *
  * Shapes: B tokens (batch × sequence), expansion n, hidden size C,
  * K = n·C, N = n² + 2n.
@@ -31,8 +33,8 @@
  * are rounded to nearest even.
  *
  * Ownership and ordering: every pointer is a DEVICE pointer owned by the
- * caller; the library never allocates, frees or keeps a pointer after a call
- * returns.  Each call only validates its arguments and enqueues kernels on
+ * caller (mhc_forward_host alone takes host activations); the library never
+ * allocates, frees or keeps a pointer after a call returns.  Each call only validates its arguments and enqueues kernels on
  * `stream` (NULL = the legacy default stream); it returns without waiting.
  *
  * Argument rules (checked on the host; a failing call launches nothing):
@@ -129,16 +131,68 @@ int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_
                        mhc_stream_t stream);
 
 /*
- * The whole forward: mhc_gemm_rms, mhc_coeffs, mhc_pre_apply and
- * mhc_post_res_apply in that order on `stream`, with the same argument rules
- * as the four calls.  F_out is an input: inside a real layer it is F(F_pre),
- * which lies outside mHC (§2.5 (2)).  X_next may be exactly X.
+ * The whole forward on `stream`, with the same argument rules and results as
+ * mhc_gemm_rms, mhc_coeffs, mhc_pre_apply and mhc_post_res_apply called in
+ * that order.  F_out is an input: inside a real layer it is F(F_pre), which
+ * lies outside mHC (§2.5 (2)), so step 4b is always a launch of its own.
+ * X_next may be exactly X.
+ *
+ * Path: for B <= 3072 steps 1-4a run as one cooperative launch (the split-K
+ * GEMM over every SM, a bounded grid barrier, then each CTA's fixed-order
+ * reduction, coefficients and F_pre), which measured faster than the
+ * four-kernel chain at those sizes; above, the chain.  Either path is
+ * deterministic; they differ in the split-K order, so Y (and what follows
+ * from it) differs between them in the last bits, within the tolerances.
  */
 int mhc_forward(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
                 float alpha_pre, float alpha_post, float alpha_res, const float *bias,
                 int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
                 float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
                 void *workspace, size_t workspace_bytes, mhc_stream_t stream);
+
+/*
+ * Bytes of DEVICE scratch mhc_forward_host needs for (B, n, C) on the current
+ * device: three chunk slots of bf16 buffers for chunks of up to 1024 tokens,
+ * the fp32 outputs (Y, r, H) of the whole batch and the forward workspace
+ * (about 0.27 GB at B=16384, n=4, C=7168).  0 when the
+ * arguments are out of range or no device is usable.
+ */
+size_t mhc_forward_host_scratch_bytes(int64_t B, int n, int64_t C);
+
+/*
+ * mhc_forward over HOST-resident activations:
+ *   X, F_out                        host inputs   (layouts as mhc_forward)
+ *   Y, r, H_pre, H_post, H_res,
+ *   F_pre, X_next                   host outputs  (X_next may be exactly X)
+ *   phi_t, bias                     DEVICE inputs (weights, resident)
+ *   scratch                         DEVICE scratch of mhc_forward_host_scratch_bytes
+ * The batch goes through the device in chunks of tokens: 256 and 512 first,
+ * then chunks of 1024 (the last of them possibly shorter), then 512 and 256,
+ * so that the first copy in and the last copy out, which nothing overlaps,
+ * are short; a batch below 2560 tokens goes in chunks of 256 (the last
+ * possibly shorter).  The copy of one chunk to the device, the forward of the
+ * previous one (mhc_forward's path for the chunk size) and the copy of the
+ * outputs before that back to the host run concurrently on two internal copy
+ * streams and `stream`.  Every copy is one cudaMemcpyAsync.  Results equal
+ * mhc_forward's on the same chunks bit for bit (tokens are independent, §2.3).
+ *
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to overlap; pageable memory is accepted and copies synchronously.
+ * The call is stream-ordered: it starts after the work already on `stream`,
+ * and work enqueued on `stream` afterwards starts only once every output is in
+ * host memory (synchronise `stream` before reading them).  Calls on one device
+ * are serialised on the library's copy streams; do not touch the host buffers
+ * or the scratch until then.
+ *
+ * Rules of mhc_forward, plus: the activation pointers must be host memory and
+ * phi_t, bias and scratch device memory (MHC_ERR_INVALID otherwise);
+ * scratch_bytes < mhc_forward_host_scratch_bytes gives MHC_ERR_WORKSPACE.
+ */
+int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                     void *scratch, size_t scratch_bytes, mhc_stream_t stream);
 
 /*
  * Size of the built-in scratch array of mhc_gemm_rms_noalloc: 16 MiB, held in

@@ -66,9 +66,9 @@ int mhc_testing_forward_chain(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mh
  * mhc_forward forced onto the small-batch path: steps 1-4a in one cooperative
  * launch (the split-K GEMM over all SMs, a bounded grid barrier, then each
  * CTA's fixed-order reduction, coefficients and F_pre), then the X_next
- * kernel.  mhc_forward takes this path by itself for B <= 128; this hook
- * takes it for any B <= 512.  Same arguments, rules and outputs as
- * mhc_forward; MHC_ERR_UNSUPPORTED for B > 512.
+ * kernel.  mhc_forward takes this path by itself for B <= 3072; this hook
+ * takes it for any B <= 4096.  Same arguments, rules and outputs as
+ * mhc_forward; MHC_ERR_UNSUPPORTED for B > 4096.
  */
 int mhc_testing_forward_decode(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F_out,
                                float alpha_pre, float alpha_post, float alpha_res,

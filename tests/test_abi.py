@@ -167,3 +167,25 @@ def test_testing_hooks_validate_on_the_host():
     args = [A, B_, C_, 0.01, 0.01, 0.01, D, -1, 4, 4, 256, E, F, G, H, I, J, 0x1_0000_0000, W,
             1 << 30, None, 50_000_000]
     assert L.mhc_testing_forward_decode_stalled(*args) == mhc.MHC_ERR_INVALID
+
+
+def test_forward_host_validates_on_the_host():
+    f = L.mhc_forward_host
+    args = [A, B_, C_, 0.01, 0.01, 0.01, D, 20, 4, 4, 256, E, F, G, H, I, J, 0x1_0000_0000, W,
+            1 << 30, None]
+    assert f(*args) == NO_DEVICE
+    a = list(args); a[8] = 0
+    assert f(*a) == mhc.MHC_OK  # empty batch
+    a = list(args); a[9] = 9
+    assert f(*a) == mhc.MHC_ERR_UNSUPPORTED
+    a = list(args); a[7] = -1
+    assert f(*a) == mhc.MHC_ERR_INVALID
+    a = list(args); a[0] = None
+    assert f(*a) == mhc.MHC_ERR_INVALID
+    a = list(args); a[18] = W + 8  # scratch misaligned
+    assert f(*a) == mhc.MHC_ERR_ALIGN
+    a = list(args); a[17] = A  # X_next == X is allowed
+    assert f(*a) == NO_DEVICE
+    a = list(args); a[16] = A  # F_pre over X is not
+    assert f(*a) == mhc.MHC_ERR_INVALID
+    assert mhc._lib.mhc_forward_host_scratch_bytes(64, 4, 256) == 0  # needs a device

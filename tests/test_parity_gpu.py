@@ -328,9 +328,10 @@ def test_forward_chain_path_small_batches(name):
 
 
 # shapes for the small-batch one-launch path: every n, ragged K blocks, ragged
-# and several token tiles (up to its 512-token limit), one CTA and all SMs
+# and several token tiles (up to 2048 of its 4096-token limit), one CTA and all SMs
 DECODE_SHAPES = ODD_SHAPES + [(1, 4, 7168), (1, 8, 7168), (128, 4, 7168), (129, 4, 7168),
-                              (300, 8, 512), (512, 4, 7168), (77, 6, 1000)]
+                              (300, 8, 512), (512, 4, 7168), (77, 6, 1000), (1100, 4, 2048),
+                              (2048, 4, 512), (2000, 8, 264)]
 
 
 @pytest.mark.parametrize("B,n,C", DECODE_SHAPES)
@@ -375,7 +376,7 @@ def test_forward_decode_in_place(path):
 
 
 def test_forward_decode_path_rejects_large_batches():
-    wl = WORKLOADS["tiny"].with_(B=513)
+    wl = WORKLOADS["tiny"].with_(B=4097)
     inp = make_inputs(wl, seed=6)
     with pytest.raises(mhc.MhcError) as ei:
         forward_gpu(inp, wl, path="decode")
