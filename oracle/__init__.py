@@ -6,7 +6,9 @@ CUDA library never does, and this package imports nothing from it.
 
 The arithmetic lives in ``mhc_oracle.c`` (plain C, double precision, one
 thread, index-order sums), a restatement of §2.1–§2.5 of the page
-"mHC 算法分析 & cutile 高效实现".  This module only marshals numpy arrays.
+"mHC 算法分析 & cutile 高效实现", plus C = rmsnorm(A) @ B of §2 of the page
+"Towards Free Normalization: Fusing Normalization into GEMM and Attention
+Kernels" (``rmsnorm_gemm``).  This module only marshals numpy arrays.
 
 Pins: every function here is checked in ``tests/test_oracle_pins.py``
 against closed forms, invariants, one-hot special cases and exact-integer
@@ -56,6 +58,7 @@ def _configure(lib):
         "oracle_post_res_apply": [vp, vp, vp, vp, i64, i32, i64, vp],
         "oracle_forward": [vp, vp, vp, i64, i32, i64, dbl, dbl, dbl, vp, i32,
                            vp, vp, vp, vp, vp, vp, vp],
+        "oracle_rmsnorm_gemm": [vp, vp, i64, i64, i64, dbl, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -193,3 +196,15 @@ def forward(X, phi, F_out, n: int, C: int, a_pre, a_post, a_res, bias, iters: in
                            *(o[k].ctypes.data for k in ("Y", "r", "H_pre", "H_post", "H_res",
                                                           "F_pre", "X_next")))
     return o
+
+
+def rmsnorm_gemm(A, Bm, eps: float = 1e-5):
+    """"Towards Free Normalization" §2: C = rmsnorm(A) @ B.  A [M, K] and Bm [K, N]
+    bf16 bits (B in its mathematical orientation) -> C [M, N] float64."""
+    A, Bm = _u16(A), _u16(Bm)
+    M, K = A.shape
+    K2, N = Bm.shape
+    assert K2 == K, (A.shape, Bm.shape)
+    C = np.zeros((M, N))
+    _load().oracle_rmsnorm_gemm(A.ctypes.data, Bm.ctypes.data, M, K, N, float(eps), C.ctypes.data)
+    return C

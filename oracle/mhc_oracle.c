@@ -18,6 +18,12 @@
  *   - H_res row i mixes into output stream i: X_next[i] = Σ_j H_res[i][j]·X[j]
  *     (§3.4 and §5.4), and "H_post^T · F_out" is the per-token outer product
  *     X_post[i][c] = H_post[i]·F_out[c] (§3.4 loop, §5.4).
+ *
+ * oracle_rmsnorm_gemm restates a second page, "Towards Free Normalization:
+ * Fusing Normalization into GEMM and Attention Kernels" (PyTorch blog), §2:
+ * C = rmsnorm(A) @ B with rmsnorm(A) = A · rstd(A) row by row and
+ * rstd = 1 / sqrt(mean of the row's squares + eps).  It is written as that
+ * definition (normalise first, then multiply), not in the page's lazy order.
  */
 #include "mhc_oracle.h"
 
@@ -186,4 +192,30 @@ void oracle_forward(const uint16_t *X, const uint16_t *phi, const uint16_t *F_ou
     oracle_coeffs(Y, r, a_pre, a_post, a_res, bias, iters, B, n, H_pre, H_post, H_res);
     oracle_pre_apply(X, H_pre, B, n, C, F_pre);
     oracle_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next);
+}
+
+/*
+ * "Towards Free Normalization", §2: C = rmsnorm(A) @ B, where every row a of
+ * A is scaled by rstd = 1 / sqrt(Σ_q a_q² / K + eps) before the product.
+ * A [M][K] bf16, Bm [K][N] bf16 (the mathematical orientation), C [M][N].
+ */
+void oracle_rmsnorm_gemm(const uint16_t *A, const uint16_t *Bm, int64_t M, int64_t K, int64_t N,
+                         double eps, double *Cout)
+{
+    double *row = (double *)malloc((size_t)(K > 0 ? K : 1) * sizeof(double));
+    for (int64_t m = 0; m < M; ++m) {
+        double ss = 0.0;
+        for (int64_t q = 0; q < K; ++q) {
+            const double a = oracle_bf16_to_f64(A[m * K + q]);
+            ss += a * a;
+        }
+        const double rstd = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t q = 0; q < K; ++q) row[q] = oracle_bf16_to_f64(A[m * K + q]) * rstd;
+        for (int64_t k = 0; k < N; ++k) {
+            double acc = 0.0;
+            for (int64_t q = 0; q < K; ++q) acc += row[q] * oracle_bf16_to_f64(Bm[q * N + k]);
+            Cout[m * N + k] = acc;
+        }
+    }
+    free(row);
 }

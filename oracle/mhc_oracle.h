@@ -57,6 +57,11 @@ void oracle_forward(const uint16_t *X, const uint16_t *phi, const uint16_t *F_ou
                     const double *bias, int iters, double *Y, double *r, double *H_pre,
                     double *H_post, double *H_res, double *F_pre, double *X_next);
 
+/* "Towards Free Normalization" §2: C = rmsnorm(A) @ B with eps inside the
+ * square root.  A [M][K] bf16 bits, Bm [K][N] bf16 bits, C [M][N] double. */
+void oracle_rmsnorm_gemm(const uint16_t *A, const uint16_t *Bm, int64_t M, int64_t K, int64_t N,
+                         double eps, double *Cout);
+
 #ifdef __cplusplus
 }
 #endif

@@ -354,4 +354,47 @@ def pin_forward_matches_steps_and_logits():
     _close(np.log(o["H_res"].reshape(B, n * n)), lazy[:, 2 * n:], 1e-12, "res log (iters=0)")
 
 
+# ------------------------------------ "Towards Free Normalization" §2
+
+
+def pin_rmsnorm_gemm_exact_rows():
+    """rstd = 1/sqrt(Σa²/K + eps) on rows whose value is exact: [1,1,1,1] and
+    [2,0,0,0] have mean square 1, so eps = 3 gives rstd = 1/2; with B = I the
+    product is the scaled rows, exactly.  A zero row stays zero."""
+    A = _bf16([[1, 1, 1, 1], [2, 0, 0, 0], [0, 0, 0, 0], [1, -1, 1, -1]])
+    I4 = _bf16(np.eye(4))
+    C = O.rmsnorm_gemm(A, I4, eps=3.0)
+    want = np.array([[0.5, 0.5, 0.5, 0.5], [1, 0, 0, 0], [0, 0, 0, 0], [0.5, -0.5, 0.5, -0.5]])
+    assert np.array_equal(C, want), C
+    # eps = 0: the same rows scaled to unit mean square
+    C0 = O.rmsnorm_gemm(A[[0, 1, 3]], I4, eps=0.0)
+    assert np.array_equal(C0, [[1, 1, 1, 1], [2, 0, 0, 0], [1, -1, 1, -1]]), C0
+
+
+def pin_rmsnorm_gemm_constant_rows():
+    """A row of constant s: rstd = 1/sqrt(s² + eps), C = s·rstd·(column sums of B)."""
+    K, N = 24, 5
+    Bm = synth.normal_bf16((K, N), 31, 2, 0.5)
+    Bf = synth.bf16_bits_to_f32(Bm).astype(np.float64)
+    for s_, eps in ((0.5, 1e-5), (-3.0, 0.25), (2.0, 0.0)):
+        A = _bf16(np.full((1, K), s_))
+        want = s_ / math.sqrt(s_ * s_ + eps) * Bf.sum(axis=0)
+        _close(O.rmsnorm_gemm(A, Bm, eps)[0], want, 1e-13, "constant row s=%g" % s_)
+
+
+def pin_rmsnorm_gemm_lazy_identity():
+    """The lazy order of the page's §2: with eps = 0, rmsnorm(A) @ B times r equals
+    A @ B, i.e. the mHC oracle's Ỹ (n = 1, so φ is K × 3) for the same A."""
+    C_, n = 40, 1
+    K, N = n * C_, n * n + 2 * n
+    X = synth.normal_bf16((7, K), 33, 0, 1.0)
+    phi = synth.normal_bf16((K, N), 33, 2, 0.2)
+    Y, r = O.gemm_rms(X, phi, n, C_)
+    Cn = O.rmsnorm_gemm(X, phi, eps=0.0)
+    _close(Cn * r[:, None], Y, 1e-12 * max(1.0, float(np.abs(Y).max())), "rmsnorm(A)@B · r = A@B")
+    # eps > 0 shrinks every row by sqrt(r² / (r² + eps)) relative to eps = 0
+    Ce = O.rmsnorm_gemm(X, phi, eps=0.3)
+    _close(Ce, Cn * (r / np.sqrt(r * r + 0.3))[:, None], 1e-12, "eps scaling")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -41,6 +41,9 @@ MUTANTS = {
                           "X_next[b * K + (int64_t)i * C + c] = x_res;"),
     "F_out index": ("oracle_bf16_to_f64(F_out[b * C + c])", "oracle_bf16_to_f64(F_out[c])"),
     "forward skips pre": ("    oracle_pre_apply(X, H_pre, B, n, C, F_pre);\n", ""),
+    "rmsnorm drops eps": ("1.0 / sqrt(ss / (double)K + eps);", "1.0 / sqrt(ss / (double)K);"),
+    "rmsnorm sum not mean": ("1.0 / sqrt(ss / (double)K + eps);", "1.0 / sqrt(ss + eps);"),
+    "rmsnorm B transposed": ("oracle_bf16_to_f64(Bm[q * N + k])", "oracle_bf16_to_f64(Bm[k * K + q])"),
 }
 
 
