@@ -346,6 +346,65 @@ def host_link_copy(h_X, h_F, h_out, X, F_out, out, stream):
     return once
 
 
+def run_rmsnorm_gemm(args) -> int:
+    """C = rmsnorm(A) @ B on one GPU: TFLOP/s of the fused kernel against the
+    measured bf16 peak, beside cuBLAS's plain A @ B and PyTorch's
+    rmsnorm-then-matmul of the same shape (context, not targets).  A, B
+    ~N(0,1), N(0,0.02²) bf16, eps 1e-5; A is larger than L2 for the default
+    shape, and every step reads it again."""
+    import torch
+
+    import gemm_rms_sinkhorn_gb300 as mhc
+    import synth
+
+    M, K, N = (int(v) for v in args.gemm.split(","))
+    dev = torch.device("cuda", 0)
+    to_dev = lambda bits: torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    A = to_dev(synth.normal_bf16((M, K), 51, 0))
+    B_t = to_dev(synth.normal_bf16((N, K), 51, 2, 0.02))
+    C = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    nbytes = mhc._lib.mhc_rmsnorm_gemm_workspace_bytes(M, K, N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev) if nbytes else None
+    stream = torch.cuda.current_stream(dev)
+    flop = 2.0 * M * N * K
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps
+
+    ours = timed(lambda: mhc.mhc_rmsnorm_gemm(A, B_t, M, K, N, 1e-5, C, ws, stream))
+    cublas = timed(lambda: torch.matmul(A, B_t.t()))
+
+    def torch_rms_mm():
+        rstd = torch.rsqrt(A.float().pow(2).mean(-1, keepdim=True) + 1e-5)
+        return torch.matmul((A.float() * rstd).to(torch.bfloat16), B_t.t())
+
+    eager = timed(torch_rms_mm)
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, src = float(json.load(f)["bf16_tflops"]), "MEASURED_PEAKS.json bf16_tflops"
+    except Exception:
+        peak, src = 1900.0, "profiling-recipe fallback 1.9 PFLOP/s"
+    tf = flop / (ours * 1e-3) / 1e12
+    line = {"mode": "rmsnorm_gemm", "M": M, "K": K, "N": N, "eps": 1e-5, "steps": args.steps,
+            "ms": ours, "tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                         "frac": tf / peak, "peak_source": src + " (of measured)"},
+            "hbm_GBps": (2.0 * (M * K + N * K + M * N)) / (ours * 1e-3) / 1e9,
+            "cublas_matmul_ms": cublas, "cublas_matmul_tflops": flop / (cublas * 1e-3) / 1e12,
+            "torch_rmsnorm_then_matmul_ms": eager}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,9 +426,13 @@ def main() -> int:
                          "steps 1-4a)")
     ap.add_argument("--tokens", type=int, default=None,
                     help="latency mode: the workload with this many tokens instead")
-    ap.add_argument("--mode", default="full", choices=["full", "kernels", "latency"],
+    ap.add_argument("--mode", default="full",
+                    choices=["full", "kernels", "latency", "rmsnorm_gemm"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
-                         "latency: microseconds per mhc_forward (stream and CUDA graph)")
+                         "latency: microseconds per mhc_forward (stream and CUDA graph); "
+                         "rmsnorm_gemm: C = rmsnorm(A) @ B (Lazy Pre-Norm) on --gemm M,K,N")
+    ap.add_argument("--gemm", default="16384,2048,2048",
+                    help="rmsnorm_gemm mode: M,K,N")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -383,6 +446,8 @@ def main() -> int:
         wl = wl.with_(name="%s_B%d" % (wl.name, args.tokens), B=args.tokens)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.mode == "rmsnorm_gemm":
+        return run_rmsnorm_gemm(args)
 
     import torch
 

@@ -47,6 +47,8 @@ _SIGS = {
                      _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
     "mhc_forward_host_scratch_bytes": ([_i64, _i32, _i64], _sz),
+    "mhc_rmsnorm_gemm_workspace_bytes": ([_i64, _i64, _i64], _sz),
+    "mhc_rmsnorm_gemm": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _sz, _vp], _i32),
     "mhc_forward_host": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_gemm_rms_noalloc": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp], _i32),
@@ -243,6 +245,26 @@ def mhc_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, it
         _hptr(r, f, "r"), _hptr(H_pre, f, "H_pre"), _hptr(H_post, f, "H_post"),
         _hptr(H_res, f, "H_res"), _hptr(F_pre, bf, "F_pre"), _hptr(X_next, bf, "X_next"), p,
         nb, _stream(stream)), "mhc_forward_host")
+
+
+def mhc_rmsnorm_gemm(A, B_t, M, K, N, eps, C, ws=None, stream=None):
+    """C = rmsnorm(A) @ B (Lazy Pre-Norm): A [M, K], B_t [N, K], C [M, N], all bf16."""
+    bf = torch.bfloat16
+    p, nb = _ws(ws)
+    _check(_lib.mhc_rmsnorm_gemm(_ptr(A, bf, "A"), _ptr(B_t, bf, "B_t"), M, K, N, eps,
+                                 _ptr(C, bf, "C"), p, nb, _stream(stream)), "mhc_rmsnorm_gemm")
+
+
+def rmsnorm_gemm(A, B_t, eps: float = 1e-5, out=None, ws=None, stream=None):
+    """``mhc_rmsnorm_gemm`` on tensors; allocates C and the workspace when not given."""
+    M, K = A.shape
+    N = B_t.shape[0]
+    C = out if out is not None else torch.empty(M, N, dtype=torch.bfloat16, device=A.device)
+    if ws is None:
+        nbytes = _lib.mhc_rmsnorm_gemm_workspace_bytes(M, K, N)
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=A.device) if nbytes else None
+    mhc_rmsnorm_gemm(A, B_t, M, K, N, eps, C, ws, stream)
+    return C
 
 
 def host_scratch(B: int, n: int, C: int, device=None) -> "torch.Tensor":

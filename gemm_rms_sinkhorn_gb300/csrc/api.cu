@@ -433,6 +433,48 @@ int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t s
     return cuda_status(launch_recip(in, out, count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// Shape rules of mhc_rmsnorm_gemm.
+static int check_rng_shape(int64_t M, int64_t K, int64_t N, float eps)
+{
+    if (M < 0 || !(eps >= 0.0f) || eps > 3.0e38f) return MHC_ERR_INVALID;
+    if (K < 8 || K % 8 != 0 || K > (int64_t{1} << 30)) return MHC_ERR_UNSUPPORTED;
+    if (N < 8 || N % 8 != 0 || N > (int64_t{1} << 24)) return MHC_ERR_UNSUPPORTED;
+    if (M >= (int64_t{1} << 31)) return MHC_ERR_UNSUPPORTED;
+    return MHC_OK;
+}
+
+size_t mhc_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N)
+{
+    if (check_rng_shape(M, K, N, 0.0f) != MHC_OK) return 0;
+    DeviceInfo info;
+    if (current_device_info(&info) != cudaSuccess) return 0;
+    return rmsnorm_gemm_workspace_bytes(M, K, N, info.num_sms);
+}
+
+int mhc_rmsnorm_gemm(const mhc_bf16 *A, const mhc_bf16 *B_t, int64_t M, int64_t K, int64_t N,
+                     float eps, mhc_bf16 *C, void *workspace, size_t workspace_bytes,
+                     mhc_stream_t stream)
+{
+    MHC_TRY(check_rng_shape(M, K, N, eps));
+    if (M == 0) return MHC_OK;
+    const Buf ins[] = {{A, bf16_bytes(M * K)}, {B_t, bf16_bytes(N * K)}};
+    Buf outs[] = {{C, bf16_bytes(M * N)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = rmsnorm_gemm_workspace_bytes(M, K, N, info.num_sms);
+    if (need > 0) {
+        if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+        outs[1].bytes = need;
+        MHC_TRY(check_ptrs(outs + 1, 1));
+        MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+    }
+    return cuda_status(launch_rmsnorm_gemm(A, B_t, M, K, N, eps, C, need > 0 ? workspace : nullptr,
+                                           info.num_sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 size_t mhc_forward_host_scratch_bytes(int64_t B, int n, int64_t C)
 {
     if (check_shape(B, n, C, true) != MHC_OK || B == 0) return 0;
@@ -478,11 +520,17 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
 int mhc_device_status(int *status)
 {
     if (status == nullptr) return MHC_ERR_INVALID;
-    int v = 0, w = 0, d = 0;
-    if (read_and_clear_device_status(&v) != cudaSuccess) return MHC_ERR_CUDA;
-    if (read_and_clear_fused_status(&w) != cudaSuccess) return MHC_ERR_CUDA;
-    if (read_and_clear_decode_status(&d) != cudaSuccess) return MHC_ERR_CUDA;
-    *status = v != MHC_OK ? v : (w != MHC_OK ? w : d);
+    int st[4] = {0, 0, 0, 0};
+    if (read_and_clear_device_status(&st[0]) != cudaSuccess) return MHC_ERR_CUDA;
+    if (read_and_clear_fused_status(&st[1]) != cudaSuccess) return MHC_ERR_CUDA;
+    if (read_and_clear_decode_status(&st[2]) != cudaSuccess) return MHC_ERR_CUDA;
+    if (read_and_clear_rmsnorm_gemm_status(&st[3]) != cudaSuccess) return MHC_ERR_CUDA;
+    *status = MHC_OK;
+    for (int v : st)
+        if (v != MHC_OK) {
+            *status = v;
+            break;
+        }
     return MHC_OK;
 }
 

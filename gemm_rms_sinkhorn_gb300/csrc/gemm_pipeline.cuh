@@ -44,8 +44,9 @@ struct Cfg {
     static constexpr int kStageBytes = kBoxA + kBoxB;
     static constexpr int kStages = BUDGET / kStageBytes;
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kTmemCols =
-        2 * NPAD <= 32 ? 32 : (2 * NPAD <= 64 ? 64 : (2 * NPAD <= 128 ? 128 : 256));
+    static constexpr int kTmemCols =  // a power of two >= 32 holding both accumulators
+        2 * NPAD <= 32 ? 32
+                       : (2 * NPAD <= 64 ? 64 : (2 * NPAD <= 128 ? 128 : (2 * NPAD <= 256 ? 256 : 512)));
     static_assert(NPAD % 16 == 0 && NPAD >= 16 && NPAD <= 256, "MMA N for M=128");
     static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kStages >= 2 && kStages <= 32, "pipeline depth (one bit per stage)");
@@ -53,7 +54,8 @@ struct Cfg {
 };
 
 struct Segment {
-    int m, k0, k1;  // token tile, K-block range [k0, k1)
+    int m, k0, k1;  // token (row) tile, K-block range [k0, k1)
+    int n = 0;      // column tile: rows [n·NPAD, (n+1)·NPAD) of the second operand
 };
 
 // Static stream-K schedule: the units (token tile, 64-wide K block), ordered
@@ -183,7 +185,7 @@ __device__ void producer(const Pipe &p, It it, const CUtensorMap *tm_x, const CU
                 ptx::mbar_arrive_expect_tx(&p.full[stage], p.stage_bytes);
                 // boxes past K read as zeros
                 ptx::tma_load_2d(a, tm_x, kb * kBK, sg.m * kBM, &p.full[stage], pol_x);
-                ptx::tma_load_2d(a + kBoxA, tm_w, kb * kBK, 0, &p.full[stage], pol_w);
+                ptx::tma_load_2d(a + kBoxA, tm_w, kb * kBK, sg.n * NPAD, &p.full[stage], pol_w);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }

@@ -135,6 +135,13 @@ cudaError_t run_forward_host(const uint16_t *X, const uint16_t *phi_t, const uin
                              float *H_post, float *H_res, uint16_t *F_pre, uint16_t *X_next,
                              void *scratch, int num_sms, cudaStream_t stream);
 
+// ---- C = rmsnorm(A) @ B, Lazy Pre-Norm (rmsnorm_gemm.cu)
+size_t rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N, int num_sms);
+cudaError_t launch_rmsnorm_gemm(const uint16_t *A, const uint16_t *B_t, int64_t M, int64_t K,
+                                int64_t N, float eps, uint16_t *C, void *workspace, int num_sms,
+                                cudaStream_t stream);
+cudaError_t read_and_clear_rmsnorm_gemm_status(int *status);
+
 // ---- steps 2-3: coefficients + Sinkhorn (coeffs.cu)
 cudaError_t launch_coeffs(const float *Y, const float *r, float a_pre, float a_post, float a_res,
                           const float *bias, int iters, int64_t B, int n, float *H_pre,

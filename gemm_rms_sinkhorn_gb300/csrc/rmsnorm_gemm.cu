@@ -1,0 +1,379 @@
+// C = rmsnorm(A) @ B with the normalisation folded into the GEMM as the page
+// "Towards Free Normalization: Fusing Normalization into GEMM and Attention
+// Kernels" (PyTorch blog), §2 "Lazy Pre-Norm", describes it:
+//
+//   rstd[m] = 1 / sqrt(Σ_q A[m][q]² / K + eps)
+//   C[m][n] = (Σ_q A[m][q]·B[q][n]) · rstd[m]        ((A·rstd) @ B = (A @ B)·rstd)
+//
+// The row sum of squares is reduced from the same shared-memory tiles the
+// tensor cores consume, by separate warps, so A leaves HBM once and the
+// normalisation costs no pass of its own; the scaling by rstd is the
+// epilogue.  It reuses the pipeline of gemm_pipeline.cuh (the mHC GEMM+RMS is
+// the skinny case of this computation) with a column-tile dimension:
+//
+//   tiles    128 rows × NT columns of C, NT = 32, 64, 128 or 256 by N, row
+//            tiles outermost so a CTA's consecutive tiles share their A rows;
+//   schedule with at least one tile per CTA, every CTA owns a contiguous run
+//            of whole tiles (no partial sums); with fewer tiles than CTAs the
+//            K blocks are split stream-K as in gemm_rms.cu, and the last CTA
+//            to finish a tile adds the partials in contributor order;
+//   epilogue the accumulator leaves TMEM 32 columns at a time, is scaled by
+//            rstd, rounded to bf16 (RNE) and stored.
+// As on the page, the square sums are computed once per column tile: the
+// redundancy runs on CUDA cores beside the tensor cores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "gemm_pipeline.cuh"
+#include "mhc_internal.h"
+#include "ptx.cuh"
+
+namespace mhc {
+namespace {
+
+using pipe::kBK;
+using pipe::kBM;
+using pipe::Segment;
+
+constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
+constexpr int kEpiThreads = 128;
+constexpr int kRingBudget = 200 * 1024;
+constexpr int kMaxFanIn = 32;  // contributors per tile when K is split
+
+__device__ int g_rng_status;
+
+template <int NT>
+struct RCfg {
+    using C = pipe::Cfg<NT, kRingBudget>;
+    static constexpr int kRstdBytes = kBM * 4;  // the last arriver's rstd of each row
+    static constexpr int kSmemBytes =
+        1024 + C::kRingBytes + pipe::kSsBytes + pipe::kBarrierBytes + kRstdBytes;
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+// Units (tile, K block), tile = row tile · n_tiles + column tile.  With
+// aligned == 1 the ranges start and end on tile boundaries.
+struct RSched {
+    int64_t tiles, total;  // tiles; tiles · kbt units
+    int kbt, n_tiles, grid, aligned;
+    __host__ __device__ int64_t lo(int c) const {
+        return aligned ? (tiles * c / grid) * kbt : total * c / grid;
+    }
+    __host__ __device__ int owner(int64_t u) const {  // CTA whose range holds unit u
+        if (aligned) return static_cast<int>(((u / kbt + 1) * grid - 1) / tiles);
+        return static_cast<int>(((u + 1) * grid - 1) / total);
+    }
+};
+
+struct RIter {
+    int64_t u, end;
+    int kbt, n_tiles;
+    __device__ bool next(Segment &s) {
+        if (u >= end) return false;
+        const int64_t t = u / kbt;
+        s.m = static_cast<int>(t / n_tiles);
+        s.n = static_cast<int>(t - static_cast<int64_t>(s.m) * n_tiles);
+        s.k0 = static_cast<int>(u - t * kbt);
+        const int64_t left = end - u;
+        s.k1 = left < kbt - s.k0 ? s.k0 + static_cast<int>(left) : kbt;
+        u += s.k1 - s.k0;
+        return true;
+    }
+};
+
+// 32 accumulator columns of this thread's row, scaled and stored as bf16.
+__device__ __forceinline__ void store_cols32(const float (&v)[32], float rstd, uint16_t *dst,
+                                             int valid)
+{
+    float t[8];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+        if (g * 8 >= valid) break;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) t[e] = v[g * 8 + e] * rstd;
+        const uint4 w = make_uint4(pack_bf16_rn(t[0], t[1]), pack_bf16_rn(t[2], t[3]),
+                                   pack_bf16_rn(t[4], t[5]), pack_bf16_rn(t[6], t[7]));
+        *reinterpret_cast<uint4 *>(dst + g * 8) = w;
+    }
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1)
+rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
+                    const __grid_constant__ CUtensorMap tm_b, int64_t M, int64_t N, int K,
+                    float eps, RSched sch, uint16_t *__restrict__ Cout, int *__restrict__ tickets,
+                    float *__restrict__ partials, uint64_t wait_limit_ns)
+{
+    using Cf = typename RCfg<NT>::C;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    pipe::Pipe p;
+    float *rstd_s = reinterpret_cast<float *>(
+        pipe::carve<NT, kRingBudget>(p, smem, &g_rng_status, wait_limit_ns));
+    uint64_t *epi_bar = p.extra;
+    volatile int *is_last = p.abort + 1;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+
+    if (threadIdx.x == 0) {
+        pipe::init_barriers(p);
+        ptx::mbar_init(epi_bar, kEpiThreads);
+        *is_last = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_a);
+        ptx::prefetch_tensormap(&tm_b);
+    }
+    if (warp == 1) ptx::tmem_alloc<Cf::kTmemCols>(p.tmem_holder);
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    p.tmem_base = *p.tmem_holder;
+    ptx::pdl_wait();
+
+    const RIter segs{sch.lo(cta), sch.lo(cta + 1), sch.kbt, sch.n_tiles};
+    const float inv_k = 1.0f / static_cast<float>(K);
+
+    if (warp == 0) {
+        if (lane == 0)  // A rows are re-read by the next column tiles: keep them in L2
+            pipe::producer<NT>(p, segs, &tm_a, &tm_b, ptx::policy_evict_normal(), -1);
+    } else if (warp == 1) {
+        if (lane == 0) pipe::mma_issuer<NT>(p, segs);
+    } else if (warp < 6) {
+        pipe::square_sum<NT>(p, segs, (warp - 2) * 32 + lane, lane);
+    } else {
+        // ----------------------------------------------- epilogue (warps 6..9)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        const int et = threadIdx.x - 192;
+        uint32_t epi_phase = 0;
+        int seg = 0;
+        RIter it = segs;
+        Segment sg;
+        while (it.next(sg)) {
+            const int acc = seg & 1;
+            const uint32_t par = (seg >> 1) & 1;
+            if (!pipe::wait(p, &p.acc_full[acc], par)) break;
+            ptx::tc_fence_after();
+            if (!pipe::wait(p, &p.ss_full[acc], par)) break;
+            const float ss = p.ss_buf[acc * kBM + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p.ss_empty[acc]);
+            ++seg;
+
+            const int64_t grow = static_cast<int64_t>(sg.m) * kBM + row;
+            const int64_t col0 = static_cast<int64_t>(sg.n) * NT;
+            const uint32_t taddr = p.tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                   static_cast<uint32_t>(acc * NT);
+            const bool whole = sg.k0 == 0 && sg.k1 == sch.kbt;
+            const int stride = NT + 1;
+            const int64_t tile = static_cast<int64_t>(sg.m) * sch.n_tiles + sg.n;
+            float *mine = partials + static_cast<int64_t>(cta + tile) * kBM * stride;
+            const float rstd = whole ? rsqrtf(ss * inv_k + eps) : 0.f;
+#pragma unroll 1
+            for (int j = 0; j < NT / 32; ++j) {
+                float v[32], t16[16];
+                ptx::tmem_ld_16(taddr + j * 32, t16);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[e] = t16[e];
+                ptx::tmem_ld_16(taddr + j * 32 + 16, t16);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) v[16 + e] = t16[e];
+                ptx::tmem_ld_wait();
+                const int64_t c0 = col0 + j * 32;
+                if (grow < M && c0 < N) {
+                    if (whole) {
+                        const int valid = N - c0 < 32 ? static_cast<int>(N - c0) : 32;
+                        store_cols32(v, rstd, Cout + grow * N + c0, valid);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mine[row * stride + j * 32 + e] = v[e];
+                    }
+                }
+                __syncwarp();  // the next tcgen05.ld is warp-collective
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p.acc_empty[acc]);
+            if (whole) continue;
+
+            // a partial: park the square sum too, take a ticket, and the last
+            // contributor adds the partials in contributor order
+            if (grow < M) mine[row * stride + NT] = ss;
+            __threadfence();
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
+            const int first = sch.owner(tile * sch.kbt);
+            const int last = sch.owner((tile + 1) * sch.kbt - 1);
+            if (et == 0) {
+                const int prev = atomicAdd(&tickets[tile], 1);
+                *is_last = (prev == last - first);
+            }
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
+            if (!*is_last) continue;
+            __threadfence();
+            const int64_t row0 = static_cast<int64_t>(sg.m) * kBM;
+            const int rows = static_cast<int>(M - row0 < kBM ? M - row0 : kBM);
+            const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
+            const float *p0 = partials + static_cast<int64_t>(first + tile) * slot_stride;
+            const int nc = last - first + 1;
+            // rstd of every row first (its square sums, in contributor order)
+            if (et < rows) {
+                float s = 0.f;
+                for (int c = 0; c < nc; ++c) s += __ldcg(p0 + c * slot_stride + et * stride + NT);
+                rstd_s[et] = rsqrtf(s * inv_k + eps);
+            }
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
+            // then the columns: thread et sums and stores 8 consecutive columns of
+            // one row (16-byte stores), rows × NT/8 items
+            const int cols = static_cast<int>(N - col0 < NT ? N - col0 : NT);
+            const int items = rows * (NT / 8);
+            for (int i = et; i < items; i += kEpiThreads) {
+                const int rr = i / (NT / 8), cc = (i - rr * (NT / 8)) * 8;
+                if (cc >= cols) continue;
+                float a8[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) a8[e] = 0.f;
+                for (int c = 0; c < nc; ++c) {
+                    const float *src = p0 + c * slot_stride + rr * stride + cc;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) a8[e] += __ldcg(src + e);
+                }
+                const float rs = rstd_s[rr];
+                const uint4 w = make_uint4(pack_bf16_rn(a8[0] * rs, a8[1] * rs),
+                                           pack_bf16_rn(a8[2] * rs, a8[3] * rs),
+                                           pack_bf16_rn(a8[4] * rs, a8[5] * rs),
+                                           pack_bf16_rn(a8[6] * rs, a8[7] * rs));
+                *reinterpret_cast<uint4 *>(Cout + (row0 + rr) * N + col0 + cc) = w;
+            }
+            if (et == 0) tickets[tile] = 0;
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;  // rstd_s is reused
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::pdl_trigger();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<Cf::kTmemCols>(p.tmem_base);
+    }
+}
+
+__global__ void zero_ints_kernel(int *p, int64_t count)
+{
+    ptx::pdl_wait();
+    ptx::pdl_trigger();
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        p[i] = 0;
+}
+
+int tile_cols(int64_t N) { return N <= 32 ? 32 : (N <= 64 ? 64 : (N <= 128 ? 128 : 256)); }
+
+RSched rng_sched(int64_t M, int64_t K, int64_t N, int num_sms)
+{
+    const int NT = tile_cols(N);
+    RSched s{};
+    s.n_tiles = static_cast<int>((N + NT - 1) / NT);
+    s.tiles = (M + kBM - 1) / kBM * s.n_tiles;
+    s.kbt = static_cast<int>((K + kBK - 1) / kBK);
+    s.total = s.tiles * s.kbt;
+    if (s.tiles >= num_sms) {  // whole tiles only
+        s.aligned = 1;
+        s.grid = num_sms;
+    } else {  // K split over the CTAs of a tile
+        s.aligned = 0;
+        int64_t g = num_sms;
+        if (g > kMaxFanIn * s.tiles) g = kMaxFanIn * s.tiles;
+        if (g > s.total) g = s.total;
+        s.grid = static_cast<int>(g < 1 ? 1 : g);
+    }
+    return s;
+}
+
+size_t tickets_bytes(int64_t tiles) { return (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256; }
+
+template <int NT>
+cudaError_t launch_nt(const CUtensorMap &ta, const CUtensorMap &tb, int64_t M, int64_t N, int K,
+                      float eps, const RSched &s, uint16_t *C, int *tickets, float *partials,
+                      int device, uint64_t limit, cudaStream_t stream)
+{
+    using R = RCfg<NT>;
+    static uint64_t configured = 0;  // one bit per device
+    static std::mutex mu;
+    if (device < 64 && !((configured >> device) & 1)) {
+        std::lock_guard<std::mutex> lock(mu);
+        cudaError_t e = cudaFuncSetAttribute(rmsnorm_gemm_kernel<NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             R::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured |= 1ull << device;
+    }
+    return launch_pdl(rmsnorm_gemm_kernel<NT>, dim3(s.grid), dim3(kThreads), R::kSmemBytes,
+                      stream, ta, tb, M, N, K, eps, s, C, tickets, partials, limit);
+}
+
+}  // namespace
+
+size_t rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N, int num_sms)
+{
+    if (M <= 0) return 0;
+    const RSched s = rng_sched(M, K, N, num_sms);
+    if (s.aligned) return 0;
+    const size_t slots = static_cast<size_t>(s.grid) + static_cast<size_t>(s.tiles);
+    return tickets_bytes(s.tiles) + slots * kBM * (tile_cols(N) + 1) * sizeof(float);
+}
+
+cudaError_t launch_rmsnorm_gemm(const uint16_t *A, const uint16_t *B_t, int64_t M, int64_t K,
+                                int64_t N, float eps, uint16_t *C, void *workspace, int num_sms,
+                                cudaStream_t stream)
+{
+    const RSched s = rng_sched(M, K, N, num_sms);
+    const int NT = tile_cols(N);
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM) ||
+        !make_tmap(&tb, B_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                   static_cast<uint32_t>(NT)))
+        return cudaErrorInvalidValue;
+    int *tickets = nullptr;
+    float *partials = nullptr;
+    cudaError_t e;
+    if (!s.aligned) {
+        tickets = static_cast<int *>(workspace);
+        partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
+                                             tickets_bytes(s.tiles));
+        const int64_t blocks = (s.tiles + 255) / 256 < 64 ? (s.tiles + 255) / 256 : 64;
+        e = launch_pdl(zero_ints_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream,
+                       tickets, s.tiles);
+        if (e != cudaSuccess) return e;
+    }
+    int device = 0;
+    if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    const int Ki = static_cast<int>(K);
+    switch (NT) {
+    case 32: return launch_nt<32>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    case 64: return launch_nt<64>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    case 128: return launch_nt<128>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    default: return launch_nt<256>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    }
+}
+
+cudaError_t read_and_clear_rmsnorm_gemm_status(int *status)
+{
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    int v = 0, zero = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_rng_status, sizeof v)) != cudaSuccess) return e;
+    if ((e = cudaMemcpyToSymbol(g_rng_status, &zero, sizeof zero)) != cudaSuccess) return e;
+    *status = v;
+    return cudaSuccess;
+}
+
+}  // namespace mhc

@@ -15,6 +15,7 @@
  *   mhc_forward         steps 1-4b on one stream (the four calls above, or for
  *                       B <= 3072 steps 1-4a in one launch, then step 4b)
  *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
+ *   mhc_rmsnorm_gemm    C = rmsnorm(A) @ B for any N (Lazy Pre-Norm, second page §2)
  *
  * Shapes: B tokens (batch × sequence), expansion n, hidden size C,
  * K = n·C, N = n² + 2n.
@@ -193,6 +194,32 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
                      int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
                      float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
                      void *scratch, size_t scratch_bytes, mhc_stream_t stream);
+
+/*
+ * C = rmsnorm(A) @ B, the "Lazy Pre-Norm" fusion of page "Towards Free
+ * Normalization: Fusing Normalization into GEMM and Attention Kernels"
+ * (PyTorch blog), §2:
+ *   rstd[m] = 1 / sqrt(Σ_q A[m][q]² / K + eps),  C[m][n] = (Σ_q A[m][q]·B[q][n])·rstd[m]
+ * which equals (A·rstd) @ B; the square sums are reduced from the tiles the
+ * tensor cores read, so A is read from HBM once, and rstd is applied to the
+ * accumulator.  mhc_gemm_rms is the skinny, eps-free case of the same
+ * computation (there the scaling is left to mhc_coeffs).
+ *
+ * Layouts (row-major, densely packed):
+ *   A    [M][K] bf16
+ *   B_t  [N][K] bf16   Bᵀ, K contiguous (a linear layer's weight [out][in])
+ *   C    [M][N] bf16   fp32 accumulation and scaling, rounded to nearest even
+ * Rules: M >= 0 (M == 0 is a no-op); 8 <= K <= 2^30 and 8 <= N <= 2^24, both
+ * multiples of 8 (MHC_ERR_UNSUPPORTED); eps finite and >= 0 (MHC_ERR_INVALID);
+ * pointers non-NULL and 16-byte aligned; C may not overlap A or B_t.
+ * workspace: mhc_rmsnorm_gemm_workspace_bytes(M, K, N) bytes of device memory
+ * (0 when every CTA gets whole output tiles; then workspace may be NULL).
+ * Results are deterministic (a fixed summation order).
+ */
+size_t mhc_rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N);
+int mhc_rmsnorm_gemm(const mhc_bf16 *A, const mhc_bf16 *B_t, int64_t M, int64_t K, int64_t N,
+                     float eps, mhc_bf16 *C, void *workspace, size_t workspace_bytes,
+                     mhc_stream_t stream);
 
 /*
  * Size of the built-in scratch array of mhc_gemm_rms_noalloc: 16 MiB, held in

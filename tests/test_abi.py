@@ -189,3 +189,18 @@ def test_forward_host_validates_on_the_host():
     a = list(args); a[16] = A  # F_pre over X is not
     assert f(*a) == mhc.MHC_ERR_INVALID
     assert mhc._lib.mhc_forward_host_scratch_bytes(64, 4, 256) == 0  # needs a device
+
+
+def test_rmsnorm_gemm_validates_on_the_host():
+    f = L.mhc_rmsnorm_gemm
+    assert f(A, B_, 0, 64, 64, 1e-5, C_, None, 0, None) == mhc.MHC_OK  # empty
+    assert f(A, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == NO_DEVICE
+    assert f(A, B_, 16, 12, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_UNSUPPORTED
+    assert f(A, B_, 16, 64, 20, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_UNSUPPORTED
+    assert f(A, B_, 16, 64, 64, -1.0, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert f(A, B_, 16, 64, 64, float("nan"), C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert f(A, B_, -1, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert f(None, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert f(A + 8, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_ALIGN
+    assert f(A, B_, 16, 64, 64, 1e-5, A + 64, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert mhc._lib.mhc_rmsnorm_gemm_workspace_bytes(16, 64, 64) == 0  # needs a device
