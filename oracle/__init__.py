@@ -59,6 +59,10 @@ def _configure(lib):
         "oracle_forward": [vp, vp, vp, i64, i32, i64, dbl, dbl, dbl, vp, i32,
                            vp, vp, vp, vp, vp, vp, vp],
         "oracle_rmsnorm_gemm": [vp, vp, i64, i64, i64, dbl, vp],
+        "oracle_gemm_rms_f64phi": [vp, vp, i64, i32, i64, vp, vp],
+        "oracle_post_res_apply_f64F": [vp, vp, vp, vp, i64, i32, i64, vp],
+        "oracle_forward_f64w": [vp, vp, vp, i64, i32, i64, dbl, dbl, dbl, vp, i32,
+                                vp, vp, vp, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -208,3 +212,41 @@ def rmsnorm_gemm(A, Bm, eps: float = 1e-5):
     C = np.zeros((M, N))
     _load().oracle_rmsnorm_gemm(A.ctypes.data, Bm.ctypes.data, M, K, N, float(eps), C.ctypes.data)
     return C
+
+
+def gemm_rms_f64phi(X, phi, n: int, C: int):
+    """§2.1–2.2 with a floating-point weight: X [B, n*C] bf16 bits, phi [n*C, N] floats."""
+    X, phi = _u16(X), _f64(phi)
+    K, N = n * C, n * n + 2 * n
+    B = X.size // K if K else 0
+    assert X.size == B * K and phi.shape == (K, N), (X.shape, phi.shape)
+    Y, r = np.zeros((B, N)), np.zeros(B)
+    _load().oracle_gemm_rms_f64phi(X.ctypes.data, phi.ctypes.data, B, n, C, Y.ctypes.data,
+                                   r.ctypes.data)
+    return Y, r
+
+
+def post_res_apply_f64F(X, F_out, H_res, H_post, n: int, C: int):
+    """§2.5 (3) with a floating-point F_out [B, C]."""
+    X, F_out, H_res, H_post = _u16(X), _f64(F_out), _f64(H_res), _f64(H_post)
+    K = n * C
+    B = X.size // K if K else 0
+    out = np.zeros((B, K))
+    _load().oracle_post_res_apply_f64F(X.ctypes.data, F_out.ctypes.data, H_res.ctypes.data,
+                                       H_post.ctypes.data, B, n, C, out.ctypes.data)
+    return out
+
+
+def forward_f64w(X, phi, F_out, n: int, C: int, a_pre, a_post, a_res, bias, iters: int):
+    """The §2 forward with φ and F_out as floating-point inputs (X bf16 bits)."""
+    X, phi, F_out, bias = _u16(X), _f64(phi), _f64(F_out), _f64(bias)
+    K, N = n * C, n * n + 2 * n
+    B = X.size // K if K else 0
+    assert phi.shape == (K, N) and F_out.size == B * C and bias.shape == (N,)
+    o = dict(Y=np.zeros((B, N)), r=np.zeros(B), H_pre=np.zeros((B, n)), H_post=np.zeros((B, n)),
+             H_res=np.zeros((B, n, n)), F_pre=np.zeros((B, C)), X_next=np.zeros((B, K)))
+    _load().oracle_forward_f64w(X.ctypes.data, phi.ctypes.data, F_out.ctypes.data, B, n, C,
+                                a_pre, a_post, a_res, bias.ctypes.data, iters,
+                                *(o[k].ctypes.data for k in ("Y", "r", "H_pre", "H_post", "H_res",
+                                                             "F_pre", "X_next")))
+    return o

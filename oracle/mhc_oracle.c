@@ -219,3 +219,57 @@ void oracle_rmsnorm_gemm(const uint16_t *A, const uint16_t *Bm, int64_t M, int64
     }
     free(row);
 }
+
+/*
+ * The page's optimised benchmark (§5) keeps the weight in fp32 (TF32 MMA) and
+ * the other inputs in fp32 while X stays bf16.  These variants take φ and F_out
+ * as doubles (exact widenings of fp32); the arithmetic is that of
+ * oracle_gemm_rms and oracle_post_res_apply.
+ */
+void oracle_gemm_rms_f64phi(const uint16_t *X, const double *phi, int64_t B, int n, int64_t C,
+                            double *Y, double *r)
+{
+    const int64_t K = (int64_t)n * C;
+    const int N = n * n + 2 * n;
+    for (int64_t b = 0; b < B; ++b) {
+        double ss = 0.0;
+        for (int64_t q = 0; q < K; ++q) {
+            const double x = oracle_bf16_to_f64(X[b * K + q]);
+            ss += x * x;
+        }
+        r[b] = sqrt(ss / (double)K);
+        for (int k = 0; k < N; ++k) {
+            double acc = 0.0;
+            for (int64_t q = 0; q < K; ++q) acc += oracle_bf16_to_f64(X[b * K + q]) * phi[q * N + k];
+            Y[b * N + k] = acc;
+        }
+    }
+}
+
+void oracle_post_res_apply_f64F(const uint16_t *X, const double *F_out, const double *H_res,
+                                const double *H_post, int64_t B, int n, int64_t C,
+                                double *X_next)
+{
+    const int64_t K = (int64_t)n * C;
+    for (int64_t b = 0; b < B; ++b) {
+        const double *h = H_res + b * n * n;
+        for (int i = 0; i < n; ++i)
+            for (int64_t c = 0; c < C; ++c) {
+                double x_res = 0.0;
+                for (int j = 0; j < n; ++j)
+                    x_res += h[i * n + j] * oracle_bf16_to_f64(X[b * K + (int64_t)j * C + c]);
+                X_next[b * K + (int64_t)i * C + c] = x_res + H_post[b * n + i] * F_out[b * C + c];
+            }
+    }
+}
+
+void oracle_forward_f64w(const uint16_t *X, const double *phi, const double *F_out, int64_t B,
+                         int n, int64_t C, double a_pre, double a_post, double a_res,
+                         const double *bias, int iters, double *Y, double *r, double *H_pre,
+                         double *H_post, double *H_res, double *F_pre, double *X_next)
+{
+    oracle_gemm_rms_f64phi(X, phi, B, n, C, Y, r);
+    oracle_coeffs(Y, r, a_pre, a_post, a_res, bias, iters, B, n, H_pre, H_post, H_res);
+    oracle_pre_apply(X, H_pre, B, n, C, F_pre);
+    oracle_post_res_apply_f64F(X, F_out, H_res, H_post, B, n, C, X_next);
+}

@@ -62,6 +62,18 @@ void oracle_forward(const uint16_t *X, const uint16_t *phi, const uint16_t *F_ou
 void oracle_rmsnorm_gemm(const uint16_t *A, const uint16_t *Bm, int64_t M, int64_t K, int64_t N,
                          double eps, double *Cout);
 
+/* fp32 weight / fp32 F_out variants (the page's §5 benchmark precision):
+ * φ [K][N] and F_out [B][C] as doubles. */
+void oracle_gemm_rms_f64phi(const uint16_t *X, const double *phi, int64_t B, int n, int64_t C,
+                            double *Y, double *r);
+void oracle_post_res_apply_f64F(const uint16_t *X, const double *F_out, const double *H_res,
+                                const double *H_post, int64_t B, int n, int64_t C,
+                                double *X_next);
+void oracle_forward_f64w(const uint16_t *X, const double *phi, const double *F_out, int64_t B,
+                         int n, int64_t C, double a_pre, double a_post, double a_res,
+                         const double *bias, int iters, double *Y, double *r, double *H_pre,
+                         double *H_post, double *H_res, double *F_pre, double *X_next);
+
 #ifdef __cplusplus
 }
 #endif

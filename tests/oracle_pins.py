@@ -397,4 +397,51 @@ def pin_rmsnorm_gemm_lazy_identity():
     _close(Ce, Cn * (r / np.sqrt(r * r + 0.3))[:, None], 1e-12, "eps scaling")
 
 
+# ------------------------------- fp32 weight / fp32 F_out (the page's §5)
+
+
+def pin_f64phi_and_f64F_agree_on_bf16_values():
+    """φ and F_out whose values are bf16: the float-input variants equal the pinned
+    bf16-input functions exactly (same values, same order)."""
+    n, C_ = 3, 20
+    K, N = n * C_, n * n + 2 * n
+    X = synth.normal_bf16((9, K), 61, 0, 1.0)
+    phi = synth.normal_bf16((K, N), 61, 2, 0.1)
+    Fo = synth.normal_bf16((9, C_), 61, 1, 1.0)
+    Y, r = O.gemm_rms(X, phi, n, C_)
+    Y2, r2 = O.gemm_rms_f64phi(X, synth.bf16_bits_to_f32(phi), n, C_)
+    assert np.array_equal(Y, Y2) and np.array_equal(r, r2)
+    Hr = O.sinkhorn(synth.normal_f32((9, n, n), 61, 9, 1.0), 20)
+    Hq = np.abs(synth.normal_f32((9, n), 61, 8, 0.5)).astype(np.float64)
+    a = O.post_res_apply(X, Fo, Hr, Hq, n, C_)
+    b = O.post_res_apply_f64F(X, synth.bf16_bits_to_f32(Fo), Hr, Hq, n, C_)
+    assert np.array_equal(a, b)
+
+
+def pin_f64phi_uses_the_fp32_bits():
+    """Integer X and φ = φ1 + 2^-12·φ2 with small integers: Ỹ = Ỹ(φ1) + 2^-12·Ỹ(φ2)
+    exactly, so the bits below bf16's mantissa count."""
+    n, C_ = 2, 12
+    K, N = n * C_, n * n + 2 * n
+    X = synth.int_bf16((5, K), 62, 0, -3, 3)
+    p1 = synth.bf16_bits_to_f32(synth.int_bf16((K, N), 62, 2, -2, 2)).astype(np.float64)
+    p2 = synth.bf16_bits_to_f32(synth.int_bf16((K, N), 62, 4, -2, 2)).astype(np.float64)
+    phi = (p1 + p2 * 2.0 ** -12).astype(np.float32).astype(np.float64)
+    assert np.array_equal(phi, p1 + p2 * 2.0 ** -12)  # exact in fp32
+    Y, _ = O.gemm_rms_f64phi(X, phi, n, C_)
+    Y1, _ = O.gemm_rms_f64phi(X, p1, n, C_)
+    Y2, _ = O.gemm_rms_f64phi(X, p2, n, C_)
+    assert np.array_equal(Y, Y1 + Y2 * 2.0 ** -12)
+
+
+def pin_f64F_post_only():
+    """H_res = 0: X_next[i] = H_post[i]·F_out with F_out's full fp32 value."""
+    n, C_ = 2, 8
+    X = synth.normal_bf16((3, n * C_), 63, 0, 1.0)
+    Fo = (synth.normal_f32((3, C_), 63, 1, 1.0) * 1.0001).astype(np.float64)
+    Hq = np.array([[0.5, 2.0], [1.0, 0.25], [1.5, 0.75]])
+    out = O.post_res_apply_f64F(X, Fo, np.zeros((3, n, n)), Hq, n, C_).reshape(3, n, C_)
+    assert np.array_equal(out, Hq[:, :, None] * Fo[:, None, :])
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -44,6 +44,9 @@ MUTANTS = {
     "rmsnorm drops eps": ("1.0 / sqrt(ss / (double)K + eps);", "1.0 / sqrt(ss / (double)K);"),
     "rmsnorm sum not mean": ("1.0 / sqrt(ss / (double)K + eps);", "1.0 / sqrt(ss + eps);"),
     "rmsnorm B transposed": ("oracle_bf16_to_f64(Bm[q * N + k])", "oracle_bf16_to_f64(Bm[k * K + q])"),
+    "f64 phi rounded to float": ("acc += oracle_bf16_to_f64(X[b * K + q]) * phi[q * N + k];",
+                                 "acc += oracle_bf16_to_f64(X[b * K + q]) * (double)(float)(phi[q * N + k] * 1.0009765625);"),
+    "f64 F_out index": ("H_post[b * n + i] * F_out[b * C + c];", "H_post[b * n + i] * F_out[c];"),
 }
 
 
