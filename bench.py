@@ -46,16 +46,19 @@ KERNEL_SOURCES = {"gemm_rms": "gemm_rms.cu", "coeffs": "coeffs.cu",
                   "pre_apply": "apply.cu", "post_res_apply": "apply.cu"}
 
 
-def algorithmic_bytes(B: int, n: int, C: int) -> dict:
-    """Compulsory HBM bytes per launch of each kernel (read once, write once)."""
+def algorithmic_bytes(B: int, n: int, C: int, precision: str = "bf16") -> dict:
+    """Compulsory HBM bytes per launch of each kernel (read once, write once).
+    precision "f32w": the weight as split bf16 pairs (2·N rows) and F_out fp32."""
     K, N = n * C, n * n + 2 * n
     X, Fc = 2 * B * K, 2 * B * C
     H = 4 * B * (2 * n + n * n)
+    wrows = 2 * N if precision == "f32w" else N
+    f_in = 4 * B * C if precision == "f32w" else Fc
     return {
-        "gemm_rms": X + 2 * N * K + 4 * B * N + 4 * B,
+        "gemm_rms": X + 2 * wrows * K + 4 * B * N + 4 * B,
         "coeffs": 4 * B * N + 4 * B + 4 * N + H,
         "pre_apply": X + 4 * B * n + Fc,
-        "post_res_apply": X + Fc + 4 * B * n * n + 4 * B * n + X,
+        "post_res_apply": X + f_in + 4 * B * n * n + 4 * B * n + X,
     }
 
 
@@ -424,6 +427,9 @@ def main() -> int:
                          "forced through its test hook: chain (four kernels), decode (the "
                          "small-batch one-launch steps 1-4a), fused (the large-batch one-kernel "
                          "steps 1-4a)")
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "f32w"],
+                    help="latency mode: f32w times mhc_forward_f32w (fp32 weight as split bf16 "
+                         "pairs, fp32 F_out) instead of the bf16 forward")
     ap.add_argument("--tokens", type=int, default=None,
                     help="latency mode: the workload with this many tokens instead")
     ap.add_argument("--mode", default="full",
@@ -482,6 +488,15 @@ def main() -> int:
     forward_call = {"auto": mhc.mhc_forward, "chain": mhc.mhc_testing_forward_chain,
                     "decode": mhc.mhc_testing_forward_decode,
                     "fused": mhc.mhc_testing_forward_fused}[args.path]
+    if args.precision == "f32w":
+        if args.mode != "latency":
+            ap.error("--precision f32w only applies to --mode latency")
+        # an fp32 weight (split once into bf16 pairs) and an fp32 F_out
+        phi32 = torch.from_numpy(synth.normal_f32((wl.N, wl.K), rank, 2, wl.phi_std)).to(dev)
+        phi_t = torch.empty(2 * wl.N, wl.K, dtype=torch.bfloat16, device=dev)
+        mhc.mhc_split_phi(phi32, n, C, phi_t)
+        F_out = torch.from_numpy(synth.normal_f32((B, C), rank, 1, wl.fout_std)).to(dev)
+        forward_call = mhc.mhc_forward_f32w
 
     def step(on_stream=None):
         forward_call(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
@@ -504,9 +519,12 @@ def main() -> int:
     if args.mode == "latency":
         sampler.stop()
         res = forward_latency(mhc, step, stream, barrier, args.steps, args.warmup)
+        alg = sum(algorithmic_bytes(B, n, C, args.precision).values())
         if rank == 0:
             print(json.dumps({"mode": "latency", "workload": wl.name, "B": B, "n": n, "C": C,
-                              "path": args.path, **res}),
+                              "path": args.path, "precision": args.precision, **res,
+                              "algorithmic_bytes": alg,
+                              "GBps_graph": alg / (res["us_per_forward_graph"] * 1e-6) / 1e9}),
                   flush=True)
         return 0
 

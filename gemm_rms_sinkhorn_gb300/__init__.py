@@ -48,6 +48,11 @@ _SIGS = {
     "mhc_device_status": ([ctypes.POINTER(_i32)], _i32),
     "mhc_forward_host_scratch_bytes": ([_i64, _i32, _i64], _sz),
     "mhc_rmsnorm_gemm_workspace_bytes": ([_i64, _i64, _i64], _sz),
+    "mhc_split_phi": ([_vp, _i32, _i64, _vp, _vp], _i32),
+    "mhc_gemm_rms_split": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_post_res_apply_f32": ([_vp, _vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
+    "mhc_forward_f32w": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_rmsnorm_gemm": ([_vp, _vp, _i64, _i64, _i64, _f32, _vp, _vp, _sz, _vp], _i32),
     "mhc_forward_host": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
@@ -245,6 +250,42 @@ def mhc_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, it
         _hptr(r, f, "r"), _hptr(H_pre, f, "H_pre"), _hptr(H_post, f, "H_post"),
         _hptr(H_res, f, "H_res"), _hptr(F_pre, bf, "F_pre"), _hptr(X_next, bf, "X_next"), p,
         nb, _stream(stream)), "mhc_forward_host")
+
+
+def mhc_split_phi(phi_t, n, C, phi_split, stream=None):
+    """fp32 phi_t [N, K] -> bf16 phi_split [2N, K] (hi, remainder interleaved)."""
+    _check(_lib.mhc_split_phi(_ptr(phi_t, torch.float32, "phi_t"), n, C,
+                              _ptr(phi_split, torch.bfloat16, "phi_split"), _stream(stream)),
+           "mhc_split_phi")
+
+
+def mhc_gemm_rms_split(X, phi_split, B, n, C, Y, r, ws, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_gemm_rms_split(_ptr(X, bf, "X"), _ptr(phi_split, bf, "phi_split"), B, n, C,
+                                   _ptr(Y, f, "Y"), _ptr(r, f, "r"), p, nb, _stream(stream)),
+           "mhc_gemm_rms_split")
+
+
+def mhc_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    _check(_lib.mhc_post_res_apply_f32(_ptr(X, bf, "X"), _ptr(F_out, f, "F_out"),
+                                       _ptr(H_res, f, "H_res"), _ptr(H_post, f, "H_post"), B, n,
+                                       C, _ptr(X_next, bf, "X_next"), _stream(stream)),
+           "mhc_post_res_apply_f32")
+
+
+def mhc_forward_f32w(X, phi_split, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                     Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    """The fp32-weight forward: phi_split from mhc_split_phi, F_out fp32 [B, C]."""
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_forward_f32w(
+        _ptr(X, bf, "X"), _ptr(phi_split, bf, "phi_split"), _ptr(F_out, f, "F_out"), alpha_pre,
+        alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n, C, _ptr(Y, f, "Y"),
+        _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"), _ptr(H_post, f, "H_post"),
+        _ptr(H_res, f, "H_res"), _ptr(F_pre, bf, "F_pre"), _ptr(X_next, bf, "X_next"), p, nb,
+        _stream(stream)), "mhc_forward_f32w")
 
 
 def mhc_rmsnorm_gemm(A, B_t, M, K, N, eps, C, ws=None, stream=None):

@@ -433,6 +433,105 @@ int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t s
     return cuda_status(launch_recip(in, out, count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+// ---------------------------------------- fp32-weight precision variant
+
+int mhc_split_phi(const float *phi_t, int n, int64_t C, mhc_bf16 *phi_split, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(1, n, C, true));
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{phi_t, f32_bytes(int64_t{N} * K)}};
+    const Buf outs[] = {{phi_split, bf16_bytes(int64_t{2} * N * K)}};
+    MHC_TRY(check_ptrs(ins, 1));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 1, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_split_phi(phi_t, n, C, phi_split,
+                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_gemm_rms_split(const mhc_bf16 *X, const mhc_bf16 *phi_split, int64_t B, int n, int64_t C,
+                       float *Y, float *r, void *workspace, size_t workspace_bytes,
+                       mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_split, bf16_bytes(int64_t{2} * N * K)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 2));
+    MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[2].bytes = need;
+    MHC_TRY(check_ptrs(outs + 2, 1));
+    MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    return cuda_status(launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_post_res_apply_f32(const mhc_bf16 *X, const float *F_out, const float *H_res,
+                           const float *H_post, int64_t B, int n, int64_t C, mhc_bf16 *X_next,
+                           mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (B == 0) return MHC_OK;
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {F_out, f32_bytes(B * C)},
+                       {H_res, f32_bytes(B * n * n)}, {H_post, f32_bytes(B * n)}};
+    const Buf outs[] = {{X_next, bf16_bytes(B * K)}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next,
+                                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                     void *workspace, size_t workspace_bytes, mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_split, bf16_bytes(int64_t{2} * N * K)},
+                       {F_out, f32_bytes(B * C)}, {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {F_pre, bf16_bytes(B * C)},
+                  {X_next, bf16_bytes(B * K)},   {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 7));
+    MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[7].bytes = need;
+    MHC_TRY(check_ptrs(outs + 7, 1));
+    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s);
+    if (e == cudaSuccess)
+        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
+                          H_post, H_res, s);
+    if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    if (e == cudaSuccess)
+        e = launch_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next, s);
+    return cuda_status(e);
+}
+
 // Shape rules of mhc_rmsnorm_gemm.
 static int check_rng_shape(int64_t M, int64_t K, int64_t N, float eps)
 {

@@ -53,9 +53,25 @@ __global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__
 // Up to n = 4 the kernel fits in 64 registers: 8 blocks of 128 threads per SM,
 // enough loads in flight to reach copy bandwidth (measured 305 µs against 312 µs
 // at 72 registers, B=16384, C=7168).  Wider n is held to 128 registers.
-template <int n>
+// Eight consecutive F_out values as fp32, from bf16 (one 128-bit load) or fp32
+// (two) storage.
+__device__ __forceinline__ void load_f8(const uint16_t *p, float (&f)[8])
+{
+    unpack8(ptx::ld_stream_v4(p), f);
+}
+__device__ __forceinline__ void load_f8(const float *p, float (&f)[8])
+{
+    const uint4 a = ptx::ld_stream_v4(p), b = ptx::ld_stream_v4(p + 4);
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+    f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+    f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+}
+
+// FT: the element type of F_out, uint16_t (bf16) or float.
+template <int n, typename FT>
 __global__ void __launch_bounds__(256, n <= 4 ? 4 : 2)
-post_res_apply_kernel(const uint16_t *X, const uint16_t *__restrict__ F_out,
+post_res_apply_kernel(const uint16_t *X, const FT *__restrict__ F_out,
                                       const float *__restrict__ H_res,
                                       const float *__restrict__ H_post, int64_t B, int64_t C,
                                       uint16_t *X_next)
@@ -86,9 +102,8 @@ post_res_apply_kernel(const uint16_t *X, const uint16_t *__restrict__ F_out,
             uint4 xv[n];
 #pragma unroll
             for (int j = 0; j < n; ++j) xv[j] = ptx::ld_stream_v4(x + j * C);
-            const uint4 fv = ptx::ld_stream_v4(F_out + b * C + c8 * 8);
             float f[8];
-            unpack8(fv, f);
+            load_f8(F_out + b * C + c8 * 8, f);
             uint16_t *y = X_next + b * n * C + c8 * 8;
 #pragma unroll
             for (int i = 0; i < n; ++i) ptx::st_stream_v4(y + i * C, post_mix8<n>(hs, i, xv, f));
@@ -110,6 +125,26 @@ dim3 apply_grid(int64_t B, int64_t C8, int threads)
     const int64_t gx = (C8 + threads - 1) / threads;
     const int64_t gy = B < kMaxGridY ? B : kMaxGridY;
     return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
+}
+
+template <typename FT>
+cudaError_t launch_post_res(const uint16_t *X, const FT *F_out, const float *H_res,
+                            const float *H_post, int64_t B, int n, int64_t C, uint16_t *X_next,
+                            cudaStream_t stream)
+{
+    const int64_t C8 = C / 8;
+    const int threads = block_threads(C8);
+    const dim3 grid = apply_grid(B, C8, threads);
+    switch (n) {
+#define MHC_CASE(k)                                                                            \
+    case k:                                                                                    \
+        return launch_pdl(post_res_apply_kernel<k, FT>, grid, dim3(threads), 0, stream, X,     \
+                          F_out, H_res, H_post, B, C, X_next);
+        MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
+        MHC_CASE(8)
+#undef MHC_CASE
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -135,20 +170,14 @@ cudaError_t launch_post_res_apply(const uint16_t *X, const uint16_t *F_out, cons
                                   const float *H_post, int64_t B, int n, int64_t C,
                                   uint16_t *X_next, cudaStream_t stream)
 {
-    const int64_t C8 = C / 8;
-    const int threads = block_threads(C8);
-    const dim3 grid = apply_grid(B, C8, threads);
-    switch (n) {
-#define MHC_CASE(k)                                                                       \
-    case k:                                                                               \
-        return launch_pdl(post_res_apply_kernel<k>, grid, dim3(threads), 0, stream, X, F_out, \
-                          H_res, H_post, B, C, X_next);
-        MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
-        MHC_CASE(8)
-#undef MHC_CASE
-    default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    return launch_post_res(X, F_out, H_res, H_post, B, n, C, X_next, stream);
+}
+
+cudaError_t launch_post_res_apply_f32(const uint16_t *X, const float *F_out, const float *H_res,
+                                      const float *H_post, int64_t B, int n, int64_t C,
+                                      uint16_t *X_next, cudaStream_t stream)
+{
+    return launch_post_res(X, F_out, H_res, H_post, B, n, C, X_next, stream);
 }
 
 }  // namespace mhc

@@ -330,6 +330,47 @@ __device__ bool take_accumulator(const Pipe &p, int seg, int q, int lane, float 
     return true;
 }
 
+// As take_accumulator, for wide accumulators: the row leaves TMEM 32 columns at
+// a time and fn(chunk, v) consumes each chunk (columns chunk·32 .. +31; past
+// NPAD the values are zero) before the next is loaded.
+template <int NPAD, typename F>
+__device__ bool take_accumulator_chunked(const Pipe &p, int seg, int q, int lane, float &ss,
+                                         F &&fn)
+{
+    const int acc = seg & 1;
+    const uint32_t par = (seg >> 1) & 1;
+    if (!wait(p, &p.acc_full[acc], par)) return false;
+    ptx::tc_fence_after();
+    const uint32_t taddr = p.tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                           static_cast<uint32_t>(acc * NPAD);
+#pragma unroll 1
+    for (int c = 0; c < (NPAD + 31) / 32; ++c) {
+        float v[32], t[16];
+        ptx::tmem_ld_16(taddr + c * 32, t);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) v[e] = t[e];
+        if (c * 32 + 16 < NPAD) {
+            ptx::tmem_ld_16(taddr + c * 32 + 16, t);
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[16 + e] = t[e];
+        } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[16 + e] = 0.f;
+        }
+        ptx::tmem_ld_wait();
+        fn(c, v);
+        __syncwarp();  // the next tcgen05.ld is warp-collective
+    }
+    ptx::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&p.acc_empty[acc]);
+    if (!wait(p, &p.ss_full[acc], par)) return false;
+    ss = p.ss_buf[acc * kBM + q * 32 + lane];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&p.ss_empty[acc]);
+    return true;
+}
+
 // Group barrier of `count` threads on an mbarrier (bounded like every wait).
 __device__ __forceinline__ bool group_sync(const Pipe &p, uint64_t *bar, uint32_t &phase)
 {

@@ -30,6 +30,7 @@
 
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
+#include "mix.cuh"
 #include "ptx.cuh"
 
 namespace mhc {
@@ -56,7 +57,10 @@ struct KCfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
-template <int NPAD>
+// kSplit: the weight operand holds every column twice, as the bf16 value
+// nearest the fp32 weight and the bf16 value nearest the remainder (rows 2k,
+// 2k+1 of φᵀ), and the epilogue adds each pair: Ỹ[k] = acc[2k] + acc[2k+1].
+template <int NPAD, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
@@ -115,32 +119,51 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         SegIter it = segs;
         Segment sg;
         while (it.next(sg)) {
-            float v[NPAD];
-            float ss;
-            if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
-            ++seg;
-
             const int64_t row0 = static_cast<int64_t>(sg.m) * kBM;
             const int64_t grow = row0 + row;
-            if (sg.k0 == 0 && sg.k1 == sch.kbt) {
-                // the whole K range of this tile is ours: write the result
-                if (grow < B) {
-                    float *y = Y + grow * N;
-#pragma unroll
-                    for (int j = 0; j < NPAD; ++j)
-                        if (j < N) y[j] = v[j];
-                    r[grow] = sqrtf(ss / static_cast<float>(K));
-                }
-                continue;
-            }
-            // partial: park [row][N+1] in this (cta, tile) slot, then take a ticket
+            const bool whole = sg.k0 == 0 && sg.k1 == sch.kbt;
             const int stride = N + 1;
             float *mine = partials + static_cast<int64_t>(cta + sg.m) * kBM * stride;
-            if (grow < B) {
+            float ss;
+            if constexpr (kSplit) {
+                // chunks of 32 accumulator columns = 16 weight columns
+                float *dst = whole ? Y + grow * N : mine + row * stride;
+                const bool ok = pipe::take_accumulator_chunked<NPAD>(
+                    p, seg, q, lane, ss, [&](int c, const float (&v)[32]) {
+                        if (grow >= B) return;
 #pragma unroll
-                for (int j = 0; j < NPAD; ++j)
-                    if (j < N) mine[row * stride + j] = v[j];
-                mine[row * stride + N] = ss;
+                        for (int e = 0; e < 16; ++e)
+                            if (c * 16 + e < N) dst[c * 16 + e] = v[2 * e] + v[2 * e + 1];
+                    });
+                if (!ok) break;
+                ++seg;
+                if (whole) {
+                    if (grow < B) r[grow] = sqrtf(ss / static_cast<float>(K));
+                    continue;
+                }
+                if (grow < B) mine[row * stride + N] = ss;
+            } else {
+                float v[NPAD];
+                if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
+                ++seg;
+                if (whole) {
+                    // the whole K range of this tile is ours: write the result
+                    if (grow < B) {
+                        float *y = Y + grow * N;
+#pragma unroll
+                        for (int j = 0; j < NPAD; ++j)
+                            if (j < N) y[j] = v[j];
+                        r[grow] = sqrtf(ss / static_cast<float>(K));
+                    }
+                    continue;
+                }
+                // partial: park [row][N+1] in this (cta, tile) slot, then take a ticket
+                if (grow < B) {
+#pragma unroll
+                    for (int j = 0; j < NPAD; ++j)
+                        if (j < N) mine[row * stride + j] = v[j];
+                    mine[row * stride + N] = ss;
+                }
             }
             __threadfence();
             if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
@@ -259,7 +282,7 @@ struct LaunchArgs {
     int64_t stall_stage;
 };
 
-template <int NPAD>
+template <int NPAD, bool kSplit>
 cudaError_t launch_cfg(const LaunchArgs &a)
 {
     using Cf = KCfg<NPAD>;
@@ -267,26 +290,58 @@ cudaError_t launch_cfg(const LaunchArgs &a)
     static std::mutex mu;
     if (a.device < 64 && !((configured >> a.device) & 1)) {
         std::lock_guard<std::mutex> lock(mu);
-        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD, kSplit>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured |= 1ull << a.device;
     }
-    return launch_pdl(gemm_rms_kernel<NPAD>, dim3(a.s.grid), dim3(kThreads),
+    return launch_pdl(gemm_rms_kernel<NPAD, kSplit>, dim3(a.s.grid), dim3(kThreads),
                       Cf::kSmemBytes, a.stream, *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r,
                       a.tickets, a.partials, a.wait_limit_ns, a.stall_stage);
 }
 
-cudaError_t dispatch(int npad, const LaunchArgs &a)
+cudaError_t dispatch(int npad, bool split, const LaunchArgs &a)
 {
+    if (split) {
+        switch (npad) {  // 2N padded: n = 1, 2 -> 16; 3 -> 32; 4 -> 48; 5 -> 80; 6 -> 96; 7 -> 128; 8 -> 160
+        case 16: return launch_cfg<16, true>(a);
+        case 32: return launch_cfg<32, true>(a);
+        case 48: return launch_cfg<48, true>(a);
+        case 80: return launch_cfg<80, true>(a);
+        case 96: return launch_cfg<96, true>(a);
+        case 128: return launch_cfg<128, true>(a);
+        case 160: return launch_cfg<160, true>(a);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (npad) {
-    case 16: return launch_cfg<16>(a);
-    case 32: return launch_cfg<32>(a);
-    case 48: return launch_cfg<48>(a);
-    case 64: return launch_cfg<64>(a);
-    case 80: return launch_cfg<80>(a);
+    case 16: return launch_cfg<16, false>(a);
+    case 32: return launch_cfg<32, false>(a);
+    case 48: return launch_cfg<48, false>(a);
+    case 64: return launch_cfg<64, false>(a);
+    case 80: return launch_cfg<80, false>(a);
     default: return cudaErrorInvalidValue;
+    }
+}
+
+// Splits an fp32 φᵀ [N][K] into bf16 rows 2k (the bf16 value nearest φ) and
+// 2k+1 (the bf16 value nearest the remainder φ - hi).
+__global__ void split_phi_kernel(const float *__restrict__ phi_t, int64_t N, int64_t K,
+                                 uint16_t *__restrict__ out)
+{
+    ptx::pdl_wait();
+    ptx::pdl_trigger();
+    const int64_t total = N * K;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t k = i / K, q = i - k * K;
+        const float v = phi_t[i];
+        const uint32_t hi2 = pack_bf16_rn(v, 0.f);
+        const float hi = __uint_as_float(hi2 << 16);
+        const uint32_t lo2 = pack_bf16_rn(v - hi, 0.f);
+        out[(2 * k) * K + q] = static_cast<uint16_t>(hi2 & 0xFFFFu);
+        out[(2 * k + 1) * K + q] = static_cast<uint16_t>(lo2 & 0xFFFFu);
     }
 }
 
@@ -335,17 +390,19 @@ size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
     return tickets_bytes(s.m_tiles) + slots * kBM * (N + 1) * sizeof(float);
 }
 
-cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
-                            int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                            cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
+static cudaError_t launch_gemm_rms_impl(const uint16_t *X, const uint16_t *phi_t, int64_t B,
+                                        int n, int64_t C, float *Y, float *r, void *workspace,
+                                        int num_sms, cudaStream_t stream, uint64_t wait_limit_ns,
+                                        int64_t stall_stage, bool split)
 {
     const int N = num_coeffs(n);
     const int64_t K = n * C;
     const Sched s = make_sched(B, n, C, num_sms);
     CUtensorMap tx, tw;
-    const int npad = npad_of(n);
+    const int wrows = split ? 2 * N : N;  // rows of the weight operand
+    const int npad = (wrows + 15) / 16 * 16;
     if (!make_tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
-        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(wrows),
                    static_cast<uint32_t>(npad)))
         return cudaErrorInvalidValue;
     int *tickets = static_cast<int *>(workspace);
@@ -359,7 +416,33 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     const LaunchArgs a{&tx, &tw, B, N, static_cast<int>(K), s, Y, r, tickets, partials, stream,
                        device, wait_limit_ns, stall_stage};
-    return dispatch(npad, a);
+    return dispatch(npad, split, a);
+}
+
+cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
+                            int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                            cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
+{
+    return launch_gemm_rms_impl(X, phi_t, B, n, C, Y, r, workspace, num_sms, stream,
+                                wait_limit_ns, stall_stage, false);
+}
+
+cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, int64_t B, int n,
+                                  int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                                  cudaStream_t stream)
+{
+    return launch_gemm_rms_impl(X, phi_split, B, n, C, Y, r, workspace, num_sms, stream,
+                                kWaitLimitNs, -1, true);
+}
+
+cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,
+                             cudaStream_t stream)
+{
+    const int64_t N = num_coeffs(n), K = n * C;
+    const int64_t need = (N * K + 255) / 256;
+    const int blocks = static_cast<int>(need < 4096 ? need : 4096);
+    return launch_pdl(split_phi_kernel, dim3(blocks), dim3(256), 0, stream, phi_t, N, K,
+                      phi_split);
 }
 
 cudaError_t read_and_clear_device_status(int *status)

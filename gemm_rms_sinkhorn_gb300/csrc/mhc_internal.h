@@ -75,6 +75,13 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
                             cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
                             int64_t stall_stage = -1);
 cudaError_t read_and_clear_device_status(int *status);
+// The fp32-weight form: phi_split [2N][K] bf16 (hi and remainder of each
+// fp32 weight column, interleaved) from launch_split_phi; the same Y and r.
+cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, int64_t B, int n,
+                                  int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                                  cudaStream_t stream);
+cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,
+                             cudaStream_t stream);
 
 // Tensor map of a 2-D bf16 tensor [rows][cols] (cols contiguous): boxes of
 // box_rows × 64 elements, 128-byte swizzle, zero fill out of bounds.
@@ -155,5 +162,9 @@ cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, i
 cudaError_t launch_post_res_apply(const uint16_t *X, const uint16_t *F_out, const float *H_res,
                                   const float *H_post, int64_t B, int n, int64_t C,
                                   uint16_t *X_next, cudaStream_t stream);
+// The same with F_out in fp32.
+cudaError_t launch_post_res_apply_f32(const uint16_t *X, const float *F_out, const float *H_res,
+                                      const float *H_post, int64_t B, int n, int64_t C,
+                                      uint16_t *X_next, cudaStream_t stream);
 
 }  // namespace mhc

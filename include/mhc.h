@@ -16,6 +16,7 @@
  *                       B <= 3072 steps 1-4a in one launch, then step 4b)
  *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
  *   mhc_rmsnorm_gemm    C = rmsnorm(A) @ B for any N (Lazy Pre-Norm, second page §2)
+ *   mhc_*_f32w / _split / _f32   the fp32-weight, fp32-F_out precision variant (§5)
  *
  * Shapes: B tokens (batch × sequence), expansion n, hidden size C,
  * K = n·C, N = n² + 2n.
@@ -194,6 +195,34 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
                      int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
                      float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
                      void *scratch, size_t scratch_bytes, mhc_stream_t stream);
+
+/*
+ * fp32-weight precision variant.  The page's optimised benchmark (§5) keeps
+ * the weight in fp32 (run as TF32 by its MMA) and F_out in fp32 while X stays
+ * bf16.  Here the fp32 φᵀ is split once into bf16 pairs and the bf16 tensor
+ * cores run twice as many columns:
+ *   mhc_split_phi       phi_t [N][K] fp32 -> phi_split [2N][K] bf16: row 2k is
+ *                       the bf16 value nearest φᵀ[k], row 2k+1 the bf16 value
+ *                       nearest the remainder; hi + lo is within about 2^-17
+ *                       relative of the fp32 weight (TF32 keeps 2^-11);
+ *   mhc_gemm_rms_split  mhc_gemm_rms with phi_split: Ỹ[k] = acc[2k] + acc[2k+1]
+ *                       (same workspace as mhc_gemm_rms);
+ *   mhc_post_res_apply_f32  mhc_post_res_apply with F_out [B][C] fp32;
+ *   mhc_forward_f32w    the four-kernel chain with both (X, F_pre, X_next bf16).
+ * Rules, layouts and status codes otherwise as the bf16 calls.
+ */
+int mhc_split_phi(const float *phi_t, int n, int64_t C, mhc_bf16 *phi_split, mhc_stream_t stream);
+int mhc_gemm_rms_split(const mhc_bf16 *X, const mhc_bf16 *phi_split, int64_t B, int n, int64_t C,
+                       float *Y, float *r, void *workspace, size_t workspace_bytes,
+                       mhc_stream_t stream);
+int mhc_post_res_apply_f32(const mhc_bf16 *X, const float *F_out, const float *H_res,
+                           const float *H_post, int64_t B, int n, int64_t C, mhc_bf16 *X_next,
+                           mhc_stream_t stream);
+int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                     void *workspace, size_t workspace_bytes, mhc_stream_t stream);
 
 /*
  * C = rmsnorm(A) @ B, the "Lazy Pre-Norm" fusion of page "Towards Free
