@@ -516,17 +516,24 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
     MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
-    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    const size_t need = forward_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[7].bytes = need;
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s);
-    if (e == cudaSuccess)
-        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
-                          H_post, H_res, s);
-    if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    cudaError_t e;
+    if (B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C)) {
+        e = launch_decode_pre(X, phi_split, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
+                              C, Y, r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
+                              kWaitLimitNs, 0, true);
+    } else {
+        e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s);
+        if (e == cudaSuccess)
+            e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
+                              H_post, H_res, s);
+        if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
+    }
     if (e == cudaSuccess)
         e = launch_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next, s);
     return cuda_status(e);

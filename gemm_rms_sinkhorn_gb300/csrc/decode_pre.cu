@@ -52,11 +52,13 @@ __device__ int g_decode_status;
 
 constexpr int npad_for(int n) { return (n * n + 2 * n + 15) / 16 * 16; }
 
-template <int n>
+// kSplit: the weight operand is the fp32-weight form (bf16 pairs, 2N rows;
+// see launch_gemm_rms_split) and the epilogue adds each pair of columns.
+template <int n, bool kSplit>
 struct DCfg {
     static constexpr int N = n * n + 2 * n;
     static constexpr int V = N + 1;  // a partial row: N sums of products, then Σx²
-    static constexpr int NPAD = npad_for(n);
+    static constexpr int NPAD = kSplit ? (2 * N + 15) / 16 * 16 : npad_for(n);
     using C = pipe::Cfg<NPAD, kRingBudget>;
     static constexpr int kBiasBytes = (N * 4 + 15) / 16 * 16;  // b, staged for phase 2
     static constexpr int kSmemBytes =
@@ -85,7 +87,7 @@ __device__ bool wait_arrivals(const uint32_t *ctr, uint32_t target, uint64_t lim
     }
 }
 
-template <int n>
+template <int n, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                   const __grid_constant__ CUtensorMap tm_w, const uint16_t *__restrict__ X,
@@ -97,7 +99,7 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                   float *__restrict__ partials, uint32_t *grid_bar, uint32_t bar_target,
                   uint64_t wait_limit_ns)
 {
-    using D = DCfg<n>;
+    using D = DCfg<n, kSplit>;
     using Cf = typename D::C;
     constexpr int N = D::N, V = D::V, NPAD = D::NPAD;
     extern __shared__ uint8_t smem_raw[];
@@ -151,18 +153,29 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
         SegIter it = segs;
         Segment sg;
         while (it.next(sg)) {
-            float v[NPAD];
-            float ss;
-            if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
-            ++seg;
             const int64_t grow = static_cast<int64_t>(sg.m) * kBM + row;
-            if (grow < B) {
-                float *mine = partials + (static_cast<int64_t>(cta + sg.m) * kBM + row) * V;
+            float *mine = partials + (static_cast<int64_t>(cta + sg.m) * kBM + row) * V;
+            float ss;
+            if constexpr (kSplit) {
+                const bool ok = pipe::take_accumulator_chunked<NPAD>(
+                    p, seg, q, lane, ss, [&](int c, const float (&v)[32]) {
+                        if (grow >= B) return;
 #pragma unroll
-                for (int j = 0; j < NPAD; ++j)
-                    if (j < N) mine[j] = v[j];
-                mine[N] = ss;
+                        for (int e = 0; e < 16; ++e)
+                            if (c * 16 + e < N) mine[c * 16 + e] = v[2 * e] + v[2 * e + 1];
+                    });
+                if (!ok) break;
+            } else {
+                float v[NPAD];
+                if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
+                if (grow < B) {
+#pragma unroll
+                    for (int j = 0; j < NPAD; ++j)
+                        if (j < N) mine[j] = v[j];
+                }
             }
+            ++seg;
+            if (grow < B) mine[N] = ss;
         }
     }
     ptx::tc_fence_before();
@@ -344,7 +357,7 @@ int decode_seg_max(const Sched &s, const TileCtas &tc)
 
 constexpr size_t kBarBytes = 256;
 
-template <int n>
+template <int n, bool kSplit>
 cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_t *X, int64_t B,
                      int64_t C, const Sched &s, const TileCtas &tc, int seg_max, float a_pre,
                      float a_post,
@@ -353,18 +366,18 @@ cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_
                      uint32_t *bar, uint32_t bar_target, uint64_t limit, int device,
                      cudaStream_t stream)
 {
-    using D = DCfg<n>;
+    using D = DCfg<n, kSplit>;
     static uint64_t configured = 0;  // one bit per device
     static std::mutex mu;
     if (device < 64 && !((configured >> device) & 1)) {
         std::lock_guard<std::mutex> lock(mu);
-        cudaError_t e = cudaFuncSetAttribute(decode_pre_kernel<n>,
+        cudaError_t e = cudaFuncSetAttribute(decode_pre_kernel<n, kSplit>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              D::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured |= 1ull << device;
     }
-    return launch_coop_pdl(decode_pre_kernel<n>, dim3(s.grid), dim3(kThreads), D::kSmemBytes,
+    return launch_coop_pdl(decode_pre_kernel<n, kSplit>, dim3(s.grid), dim3(kThreads), D::kSmemBytes,
                            stream, tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias,
                            iters,
                            Y, r, H_pre, H_post, H_res, F_pre, partials, bar, bar_target, limit);
@@ -389,7 +402,8 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
                               float a_res, const float *bias, int iters, int64_t B, int n,
                               int64_t C, float *Y, float *r, float *H_pre, float *H_post,
                               float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
-                              cudaStream_t stream, uint64_t wait_limit_ns, int barrier_extra)
+                              cudaStream_t stream, uint64_t wait_limit_ns, int barrier_extra,
+                              bool split)
 {
     if (!decode_pre_eligible(B, n, C)) return cudaErrorInvalidValue;
     const int N = num_coeffs(n);
@@ -398,9 +412,10 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
     const TileCtas tc = tile_ctas(s);
     const int seg_max = decode_seg_max(s, tc);
     CUtensorMap tx, tw;
+    const int wrows = split ? 2 * N : N;
     if (!make_tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
-        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
-                   static_cast<uint32_t>(npad_for(n))))
+        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(wrows),
+                   static_cast<uint32_t>((wrows + 15) / 16 * 16)))
         return cudaErrorInvalidValue;
     uint32_t *bar = static_cast<uint32_t *>(workspace);
     float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kBarBytes);
@@ -412,10 +427,13 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
     switch (n) {
 #define MHC_CASE(k)                                                                            \
     case k:                                                                                    \
-        return launch_n<k>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias, iters,  \
-                           Y, r,                                                                \
-                           H_pre, H_post, H_res, F_pre, partials, bar, target, wait_limit_ns,   \
-                           device, stream);
+        return split ? launch_n<k, true>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, \
+                                         bias, iters, Y, r, H_pre, H_post, H_res, F_pre,       \
+                                         partials, bar, target, wait_limit_ns, device, stream) \
+                     : launch_n<k, false>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post,      \
+                                          a_res, bias, iters, Y, r, H_pre, H_post, H_res,      \
+                                          F_pre, partials, bar, target, wait_limit_ns, device, \
+                                          stream);
         MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
         MHC_CASE(8)
 #undef MHC_CASE

@@ -208,7 +208,10 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
  *   mhc_gemm_rms_split  mhc_gemm_rms with phi_split: Ỹ[k] = acc[2k] + acc[2k+1]
  *                       (same workspace as mhc_gemm_rms);
  *   mhc_post_res_apply_f32  mhc_post_res_apply with F_out [B][C] fp32;
- *   mhc_forward_f32w    the four-kernel chain with both (X, F_pre, X_next bf16).
+ *   mhc_forward_f32w    the forward with both (X, F_pre, X_next bf16): like
+ *                       mhc_forward, steps 1-4a in one launch for B <= 3072,
+ *                       else the four-kernel chain; workspace of
+ *                       mhc_workspace_bytes.
  * Rules, layouts and status codes otherwise as the bf16 calls.
  */
 int mhc_split_phi(const float *phi_t, int n, int64_t C, mhc_bf16 *phi_split, mhc_stream_t stream);
