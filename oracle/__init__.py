@@ -48,6 +48,8 @@ def _configure(lib):
     vp, i64, i32, dbl = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
     lib.oracle_bf16_to_f64.argtypes = [ctypes.c_uint16]
     lib.oracle_bf16_to_f64.restype = dbl
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f64.restype = dbl
     sig = {
         "oracle_gemm_rms": [vp, vp, i64, i32, i64, vp, vp],
         "oracle_scale_bias": [vp, vp, dbl, dbl, dbl, vp, i64, i32, vp],
@@ -62,6 +64,8 @@ def _configure(lib):
         "oracle_gemm_rms_f64phi": [vp, vp, i64, i32, i64, vp, vp],
         "oracle_post_res_apply_f64F": [vp, vp, vp, vp, i64, i32, i64, vp],
         "oracle_forward_f64w": [vp, vp, vp, i64, i32, i64, dbl, dbl, dbl, vp, i32,
+                                vp, vp, vp, vp, vp, vp, vp],
+        "oracle_forward_e4m3": [vp, vp, vp, i64, i32, i64, dbl, dbl, dbl, vp, i32,
                                 vp, vp, vp, vp, vp, vp, vp],
     }
     for name, args in sig.items():
@@ -246,6 +250,28 @@ def forward_f64w(X, phi, F_out, n: int, C: int, a_pre, a_post, a_res, bias, iter
     o = dict(Y=np.zeros((B, N)), r=np.zeros(B), H_pre=np.zeros((B, n)), H_post=np.zeros((B, n)),
              H_res=np.zeros((B, n, n)), F_pre=np.zeros((B, C)), X_next=np.zeros((B, K)))
     _load().oracle_forward_f64w(X.ctypes.data, phi.ctypes.data, F_out.ctypes.data, B, n, C,
+                                a_pre, a_post, a_res, bias.ctypes.data, iters,
+                                *(o[k].ctypes.data for k in ("Y", "r", "H_pre", "H_post", "H_res",
+                                                             "F_pre", "X_next")))
+    return o
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    lib = _load()
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_e4m3_to_f64(int(v)) for v in c.ravel()]).reshape(c.shape)
+
+
+def forward_e4m3(X, phi, F_out, n: int, C: int, a_pre, a_post, a_res, bias, iters: int):
+    """The §2 forward on e4m3 inputs: X [B, n*C], phi [n*C, N], F_out [B, C] uint8 codes."""
+    X, phi, F_out = (np.ascontiguousarray(a, dtype=np.uint8) for a in (X, phi, F_out))
+    bias = _f64(bias)
+    K, N = n * C, n * n + 2 * n
+    B = X.size // K if K else 0
+    assert phi.shape == (K, N) and F_out.size == B * C and bias.shape == (N,)
+    o = dict(Y=np.zeros((B, N)), r=np.zeros(B), H_pre=np.zeros((B, n)), H_post=np.zeros((B, n)),
+             H_res=np.zeros((B, n, n)), F_pre=np.zeros((B, C)), X_next=np.zeros((B, K)))
+    _load().oracle_forward_e4m3(X.ctypes.data, phi.ctypes.data, F_out.ctypes.data, B, n, C,
                                 a_pre, a_post, a_res, bias.ctypes.data, iters,
                                 *(o[k].ctypes.data for k in ("Y", "r", "H_pre", "H_post", "H_res",
                                                              "F_pre", "X_next")))

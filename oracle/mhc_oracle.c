@@ -273,3 +273,76 @@ void oracle_forward_f64w(const uint16_t *X, const double *phi, const double *F_o
     oracle_pre_apply(X, H_pre, B, n, C, F_pre);
     oracle_post_res_apply_f64F(X, F_out, H_res, H_post, B, n, C, X_next);
 }
+
+/*
+ * The page's first benchmark (§4) runs the path in fp8 e4m3.  e4m3 (the OCP
+ * 8-bit format E4M3): sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities, S.1111.111 is NaN; exponent field 0 holds subnormals m·2^-9.
+ */
+double oracle_e4m3_to_f64(uint8_t b)
+{
+    const double s = (b & 0x80) ? -1.0 : 1.0;
+    const int e = (b >> 3) & 0xF, m = b & 7;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) return s * ldexp((double)m, -9);
+    return s * ldexp(1.0 + m / 8.0, e - 7);
+}
+
+/* The steps of §2 on decoded (double) inputs; X [B][K], phi [K][N], F_out [B][C]. */
+static void gemm_rms_f64(const double *X, const double *phi, int64_t B, int n, int64_t C,
+                         double *Y, double *r)
+{
+    const int64_t K = (int64_t)n * C;
+    const int N = n * n + 2 * n;
+    for (int64_t b = 0; b < B; ++b) {
+        double ss = 0.0;
+        for (int64_t q = 0; q < K; ++q) ss += X[b * K + q] * X[b * K + q];
+        r[b] = sqrt(ss / (double)K);
+        for (int k = 0; k < N; ++k) {
+            double acc = 0.0;
+            for (int64_t q = 0; q < K; ++q) acc += X[b * K + q] * phi[q * N + k];
+            Y[b * N + k] = acc;
+        }
+    }
+}
+
+static void apply_f64(const double *X, const double *F_out, const double *H_pre,
+                      const double *H_post, const double *H_res, int64_t B, int n, int64_t C,
+                      double *F_pre, double *X_next)
+{
+    const int64_t K = (int64_t)n * C;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t c = 0; c < C; ++c) {
+            double f = 0.0;
+            for (int i = 0; i < n; ++i) f += H_pre[b * n + i] * X[b * K + (int64_t)i * C + c];
+            F_pre[b * C + c] = f;
+            for (int i = 0; i < n; ++i) {
+                double x_res = 0.0;
+                for (int j = 0; j < n; ++j)
+                    x_res += H_res[b * n * n + i * n + j] * X[b * K + (int64_t)j * C + c];
+                X_next[b * K + (int64_t)i * C + c] = x_res + H_post[b * n + i] * F_out[b * C + c];
+            }
+        }
+}
+
+/* The whole forward with X, φ [K][N] and F_out given as e4m3 codes. */
+void oracle_forward_e4m3(const uint8_t *X, const uint8_t *phi, const uint8_t *F_out, int64_t B,
+                         int n, int64_t C, double a_pre, double a_post, double a_res,
+                         const double *bias, int iters, double *Y, double *r, double *H_pre,
+                         double *H_post, double *H_res, double *F_pre, double *X_next)
+{
+    const int64_t K = (int64_t)n * C;
+    const int N = n * n + 2 * n;
+    double *Xd = (double *)malloc((size_t)(B * K > 0 ? B * K : 1) * sizeof(double));
+    double *Pd = (double *)malloc((size_t)(K * N > 0 ? K * N : 1) * sizeof(double));
+    double *Fd = (double *)malloc((size_t)(B * C > 0 ? B * C : 1) * sizeof(double));
+    for (int64_t i = 0; i < B * K; ++i) Xd[i] = oracle_e4m3_to_f64(X[i]);
+    for (int64_t i = 0; i < K * N; ++i) Pd[i] = oracle_e4m3_to_f64(phi[i]);
+    for (int64_t i = 0; i < B * C; ++i) Fd[i] = oracle_e4m3_to_f64(F_out[i]);
+    gemm_rms_f64(Xd, Pd, B, n, C, Y, r);
+    oracle_coeffs(Y, r, a_pre, a_post, a_res, bias, iters, B, n, H_pre, H_post, H_res);
+    apply_f64(Xd, Fd, H_pre, H_post, H_res, B, n, C, F_pre, X_next);
+    free(Xd);
+    free(Pd);
+    free(Fd);
+}

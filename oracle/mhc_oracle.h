@@ -74,6 +74,14 @@ void oracle_forward_f64w(const uint16_t *X, const double *phi, const double *F_o
                          const double *bias, int iters, double *Y, double *r, double *H_pre,
                          double *H_post, double *H_res, double *F_pre, double *X_next);
 
+/* fp8 e4m3 (the page's §4 benchmark precision): decode, and the forward with
+ * X [B][K], φ [K][N], F_out [B][C] as e4m3 codes. */
+double oracle_e4m3_to_f64(uint8_t b);
+void oracle_forward_e4m3(const uint8_t *X, const uint8_t *phi, const uint8_t *F_out, int64_t B,
+                         int n, int64_t C, double a_pre, double a_post, double a_res,
+                         const double *bias, int iters, double *Y, double *r, double *H_pre,
+                         double *H_post, double *H_res, double *F_pre, double *X_next);
+
 #ifdef __cplusplus
 }
 #endif

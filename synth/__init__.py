@@ -113,3 +113,61 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
     r[nan] = ((u[nan] >> 16) | 0x40).astype(np.uint16)
     return r
+
+
+# ---------------------------------------------------------------- fp8 e4m3
+# OCP 8-bit floating point E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits;
+# no infinities, S.1111.111 is NaN, largest finite 448, subnormals m·2^-9.
+
+
+def _e4m3_table() -> np.ndarray:
+    v = np.empty(256, dtype=np.float64)
+    for c in range(256):
+        s = -1.0 if c & 0x80 else 1.0
+        e, m = (c >> 3) & 0xF, c & 7
+        if e == 15 and m == 7:
+            v[c] = np.nan
+        elif e == 0:
+            v[c] = s * m * 2.0 ** -9
+        else:
+            v[c] = s * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return v
+
+
+_E4M3 = _e4m3_table()
+
+
+def e4m3_bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    """Exact decoding of e4m3 codes (uint8) to float32."""
+    return _E4M3[np.ascontiguousarray(bits, dtype=np.uint8)].astype(np.float32)
+
+
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> e4m3 codes: round to nearest, ties to even; finite values past
+    448 saturate to ±448; NaN -> 0x7F (the conversion PTX calls rn.satfinite)."""
+    x = np.ascontiguousarray(x, dtype=np.float32).astype(np.float64)
+    a = np.abs(x)
+    sign = np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    code = np.zeros(x.shape, dtype=np.int64)
+    sub = a < 2.0 ** -6
+    q = np.rint(a[sub] / 2.0 ** -9).astype(np.int64)  # 8 -> the smallest normal, code 8
+    code[sub] = q
+    nrm = ~sub & np.isfinite(a)
+    mant, ex = np.frexp(a[nrm])  # a = mant·2^ex, mant in [0.5, 1)
+    e = ex - 1                   # a = (2·mant)·2^e, 2·mant in [1, 2)
+    mq = np.rint((2.0 * mant - 1.0) * 8.0).astype(np.int64)
+    e = np.where(mq == 8, e + 1, e)
+    mq = np.where(mq == 8, 0, mq)
+    field = e + 7
+    over = (field > 15) | ((field == 15) & (mq == 7))
+    c = np.where(over, (15 << 3) | 6, (np.clip(field, 1, 15) << 3) | mq)
+    code[nrm] = c
+    code[~np.isfinite(a)] = np.where(np.isnan(a[~np.isfinite(a)]), 0x7F, (15 << 3) | 6)
+    out = code.astype(np.uint8) | sign
+    out[np.isnan(x)] = 0x7F
+    return out
+
+
+def normal_e4m3(shape, seed: int, tid: int, std: float = 1.0, nthreads: int = 0) -> np.ndarray:
+    """N(0, std²) rounded to e4m3 codes (uint8)."""
+    return f32_to_e4m3_bits(normal_f32(shape, seed, tid, std, nthreads))

@@ -444,4 +444,36 @@ def pin_f64F_post_only():
     assert np.array_equal(out, Hq[:, :, None] * Fo[:, None, :])
 
 
+# ------------------------------------------- fp8 e4m3 (the page's §4)
+
+
+def pin_e4m3_decode_values():
+    """Codes of the E4M3 format: 0x38 = 1, 0x7E = 448 (largest), 0x08 = 2^-6 (smallest
+    normal), 0x01 = 2^-9 (smallest subnormal), 0x3C = 1.5, 0xC4 = -3, 0x7F NaN, 0x80 = -0."""
+    got = O.e4m3_to_f64([0x38, 0x7E, 0x08, 0x01, 0x3C, 0xC4, 0x00, 0x07, 0x77])
+    assert got.tolist() == [1.0, 448.0, 2.0 ** -6, 2.0 ** -9, 1.5, -3.0, 0.0, 7 * 2.0 ** -9, 240.0]
+    assert math.isnan(O.e4m3_to_f64([0x7F])[0]) and math.isnan(O.e4m3_to_f64([0xFF])[0])
+    assert math.copysign(1.0, O.e4m3_to_f64([0x80])[0]) == -1.0
+
+
+def pin_forward_e4m3_equals_bf16_on_shared_values():
+    """Inputs whose values are exact in both e4m3 and bf16 (multiples of 1/4 up to 3,
+    0.0625·k for φ): the e4m3 forward equals the pinned bf16 forward exactly."""
+    n, C_ = 3, 16
+    K, N = n * C_, n * n + 2 * n
+    X = synth.int_bf16((6, K), 64, 0, -12, 12)
+    Fo = synth.int_bf16((6, C_), 64, 1, -12, 12)
+    phi = synth.int_bf16((K, N), 64, 2, -8, 8)
+    q = lambda bits, s: (synth.bf16_bits_to_f32(bits) * s).astype(np.float32)
+    Xv, Fv, Pv = q(X, 0.25), q(Fo, 0.25), q(phi, 0.0625)
+    bias = synth.normal_f32(N, 64, 3, 0.1).astype(np.float64)
+    args = (n, C_, 0.5, 0.7, 0.9, bias, 20)
+    a = O.forward(synth.f32_to_bf16_bits(Xv), synth.f32_to_bf16_bits(Pv),
+                  synth.f32_to_bf16_bits(Fv), *args)
+    b = O.forward_e4m3(synth.f32_to_e4m3_bits(Xv), synth.f32_to_e4m3_bits(Pv),
+                       synth.f32_to_e4m3_bits(Fv), *args)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -47,6 +47,9 @@ MUTANTS = {
     "f64 phi rounded to float": ("acc += oracle_bf16_to_f64(X[b * K + q]) * phi[q * N + k];",
                                  "acc += oracle_bf16_to_f64(X[b * K + q]) * (double)(float)(phi[q * N + k] * 1.0009765625);"),
     "f64 F_out index": ("H_post[b * n + i] * F_out[b * C + c];", "H_post[b * n + i] * F_out[c];"),
+    "e4m3 exponent bias": ("return s * ldexp(1.0 + m / 8.0, e - 7);", "return s * ldexp(1.0 + m / 8.0, e - 8);"),
+    "e4m3 subnormal scale": ("return s * ldexp((double)m, -9);", "return s * ldexp((double)m, -10);"),
+    "e4m3 F_pre drops a stream": ("for (int i = 0; i < n; ++i) f += H_pre[b * n + i]", "for (int i = 1; i < n; ++i) f += H_pre[b * n + i]"),
 }
 
 

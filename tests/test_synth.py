@@ -54,3 +54,24 @@ def test_bf16_rounding_round_trip():
     got = synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(x))
     # ties to even: 1+2^-8 -> 1.0, 1+3*2^-8 -> 1+2^-6
     assert got[0] == 1.0 and got[1] == 1.0 and got[2] == 1.0 + 2 ** -6 and got[3] == -3.5
+
+
+def test_e4m3_codec_round_trip_and_ties():
+    import numpy as np
+    import synth
+    codes = np.arange(256, dtype=np.uint8)
+    vals = synth.e4m3_bits_to_f32(codes)
+    finite = ~np.isnan(vals)
+    assert np.array_equal(synth.f32_to_e4m3_bits(vals[finite]), codes[finite])
+    assert vals[0x38] == 1.0 and vals[0x7E] == 448.0 and vals[0x01] == 2.0 ** -9
+    assert vals[0x08] == 2.0 ** -6 and vals[0xB8] == -1.0 and np.isnan(vals[0x7F])
+    # midpoints between neighbouring positive codes go to the even code
+    pos = vals[:0x7F].astype(np.float64)
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(np.float32)
+    got = synth.f32_to_e4m3_bits(mids)
+    lo = np.arange(0, 0x7E)
+    want = np.where(lo % 2 == 0, lo, lo + 1)
+    assert np.array_equal(got, want.astype(np.uint8))
+    # saturation and NaN
+    assert synth.f32_to_e4m3_bits(np.array([1e6, -500.0, np.inf], np.float32)).tolist() == [0x7E, 0xFE, 0x7E]
+    assert synth.f32_to_e4m3_bits(np.array([np.nan], np.float32))[0] == 0x7F
