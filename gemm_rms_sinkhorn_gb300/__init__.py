@@ -49,6 +49,11 @@ _SIGS = {
     "mhc_forward_host_scratch_bytes": ([_i64, _i32, _i64], _sz),
     "mhc_rmsnorm_gemm_workspace_bytes": ([_i64, _i64, _i64], _sz),
     "mhc_split_phi": ([_vp, _i32, _i64, _vp, _vp], _i32),
+    "mhc_gemm_rms_e4m3": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp], _i32),
+    "mhc_pre_apply_e4m3": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
+    "mhc_post_res_apply_e4m3": ([_vp, _vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
+    "mhc_forward_e4m3": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
+                          _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_gemm_rms_split": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_post_res_apply_f32": ([_vp, _vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
     "mhc_forward_f32w": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
@@ -250,6 +255,53 @@ def mhc_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, it
         _hptr(r, f, "r"), _hptr(H_pre, f, "H_pre"), _hptr(H_post, f, "H_post"),
         _hptr(H_res, f, "H_res"), _hptr(F_pre, bf, "F_pre"), _hptr(X_next, bf, "X_next"), p,
         nb, _stream(stream)), "mhc_forward_host")
+
+
+def _ptr8(t, name):
+    """Device pointer of a contiguous CUDA tensor of e4m3 codes (uint8 or float8_e4m3fn)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype not in (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8)):
+        raise TypeError("%s must be uint8 or float8_e4m3fn, got %s" % (name, t.dtype))
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous CUDA tensor" % name)
+    return t.data_ptr()
+
+
+def mhc_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, ws, stream=None):
+    f = torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_gemm_rms_e4m3(_ptr8(X, "X"), _ptr8(phi_t, "phi_t"), B, n, C,
+                                  _ptr(Y, f, "Y"), _ptr(r, f, "r"), p, nb, _stream(stream)),
+           "mhc_gemm_rms_e4m3")
+
+
+def mhc_pre_apply_e4m3(X, H_pre, B, n, C, F_pre, stream=None):
+    _check(_lib.mhc_pre_apply_e4m3(_ptr8(X, "X"), _ptr(H_pre, torch.float32, "H_pre"), B, n, C,
+                                   _ptr8(F_pre, "F_pre"), _stream(stream)), "mhc_pre_apply_e4m3")
+
+
+def mhc_post_res_apply_e4m3(X, F_out, H_res, H_post, B, n, C, X_next, stream=None):
+    f = torch.float32
+    _check(_lib.mhc_post_res_apply_e4m3(_ptr8(X, "X"), _ptr8(F_out, "F_out"),
+                                        _ptr(H_res, f, "H_res"), _ptr(H_post, f, "H_post"), B, n,
+                                        C, _ptr8(X_next, "X_next"), _stream(stream)),
+           "mhc_post_res_apply_e4m3")
+
+
+def mhc_forward_e4m3(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,
+                     Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
+    """The fp8 forward: X, phi_t, F_out, F_pre, X_next as e4m3 codes."""
+    f = torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_forward_e4m3(
+        _ptr8(X, "X"), _ptr8(phi_t, "phi_t"), _ptr8(F_out, "F_out"), alpha_pre, alpha_post,
+        alpha_res, _ptr(bias, f, "bias"), iters, B, n, C, _ptr(Y, f, "Y"), _ptr(r, f, "r"),
+        _ptr(H_pre, f, "H_pre"), _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"),
+        _ptr8(F_pre, "F_pre"), _ptr8(X_next, "X_next"), p, nb, _stream(stream)),
+        "mhc_forward_e4m3")
 
 
 def mhc_split_phi(phi_t, n, C, phi_split, stream=None):

@@ -539,6 +539,113 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
     return cuda_status(e);
 }
 
+// -------------------------------------------------- fp8 e4m3 variant
+
+static int check_e4m3_shape(int64_t B, int n, int64_t C)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (C % 16 != 0) return MHC_ERR_UNSUPPORTED;  // 16 channels per 128-bit access
+    return MHC_OK;
+}
+
+int mhc_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n, int64_t C,
+                      float *Y, float *r, void *workspace, size_t workspace_bytes,
+                      mhc_stream_t stream)
+{
+    MHC_TRY(check_e4m3_shape(B, n, C));
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, static_cast<size_t>(B * K)}, {phi_t, static_cast<size_t>(N * K)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)}, {r, f32_bytes(B)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 2));
+    MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[2].bytes = need;
+    MHC_TRY(check_ptrs(outs + 2, 1));
+    MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    return cuda_status(launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_pre_apply_e4m3(const uint8_t *X, const float *H_pre, int64_t B, int n, int64_t C,
+                       uint8_t *F_pre, mhc_stream_t stream)
+{
+    MHC_TRY(check_e4m3_shape(B, n, C));
+    if (B == 0) return MHC_OK;
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, static_cast<size_t>(B * K)}, {H_pre, f32_bytes(B * n)}};
+    const Buf outs[] = {{F_pre, static_cast<size_t>(B * C)}};
+    MHC_TRY(check_ptrs(ins, 2));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_pre_apply_e4m3(X, H_pre, B, n, C, F_pre,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_post_res_apply_e4m3(const uint8_t *X, const uint8_t *F_out, const float *H_res,
+                            const float *H_post, int64_t B, int n, int64_t C, uint8_t *X_next,
+                            mhc_stream_t stream)
+{
+    MHC_TRY(check_e4m3_shape(B, n, C));
+    if (B == 0) return MHC_OK;
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, static_cast<size_t>(B * K)}, {F_out, static_cast<size_t>(B * C)},
+                       {H_res, f32_bytes(B * n * n)}, {H_post, f32_bytes(B * n)}};
+    const Buf outs[] = {{X_next, static_cast<size_t>(B * K)}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 1));
+    MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    return cuda_status(launch_post_res_apply_e4m3(X, F_out, H_res, H_post, B, n, C, X_next,
+                                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_forward_e4m3(const uint8_t *X, const uint8_t *phi_t, const uint8_t *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, uint8_t *F_pre, uint8_t *X_next,
+                     void *workspace, size_t workspace_bytes, mhc_stream_t stream)
+{
+    MHC_TRY(check_e4m3_shape(B, n, C));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, static_cast<size_t>(B * K)}, {phi_t, static_cast<size_t>(N * K)},
+                       {F_out, static_cast<size_t>(B * C)}, {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},        {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {F_pre, static_cast<size_t>(B * C)},
+                  {X_next, static_cast<size_t>(B * K)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 4));
+    MHC_TRY(check_ptrs(outs, 7));
+    MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[7].bytes = need;
+    MHC_TRY(check_ptrs(outs + 7, 1));
+    MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
+    if (e == cudaSuccess)
+        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
+                          H_post, H_res, s);
+    if (e == cudaSuccess) e = launch_pre_apply_e4m3(X, H_pre, B, n, C, F_pre, s);
+    if (e == cudaSuccess)
+        e = launch_post_res_apply_e4m3(X, F_out, H_res, H_post, B, n, C, X_next, s);
+    return cuda_status(e);
+}
+
 // Shape rules of mhc_rmsnorm_gemm.
 static int check_rng_shape(int64_t M, int64_t K, int64_t N, float eps)
 {

@@ -34,6 +34,10 @@ constexpr int kStatusTimeout = -5;  // MHC_ERR_TIMEOUT
 constexpr int kBarrierBytes = 512;
 constexpr int kSsBytes = 2 * kBM * 4;  // square-sum hand-over, double-buffered
 constexpr int kBoxABytes = kBM * kBK * 2;  // one 128 × 64 bf16 box of X
+// K elements per stage: a 128-byte swizzle row holds 64 bf16 or 128 e4m3
+// values, so an 8-bit stage has the bf16 stage's bytes and layout.
+template <bool kFp8>
+constexpr int kKPerStage = kFp8 ? 2 * kBK : kBK;
 
 // Stage geometry for MMA width NPAD (N padded to 16) and a shared-memory
 // budget for the stage ring.
@@ -162,10 +166,11 @@ __device__ __forceinline__ bool wait(const Pipe &p, uint64_t *bar, uint32_t pari
 // ------------------------------------------------------------ producer
 // One thread.  stall_stage >= 0 is a test hook: that stage (counted over the
 // thread's whole run) is left unfilled so the consumers' waits run out.
-template <int NPAD, typename It>
+template <int NPAD, typename It, bool kFp8 = false>
 __device__ void producer(const Pipe &p, It it, const CUtensorMap *tm_x, const CUtensorMap *tm_w,
                          uint64_t pol_x, int64_t stall_stage)
 {
+    constexpr int kKS = kKPerStage<kFp8>;
     constexpr int kBoxA = kBoxABytes;
     const uint64_t pol_w = ptx::policy_evict_last();  // φ is re-read by every CTA
     int stage = 0;
@@ -184,8 +189,8 @@ __device__ void producer(const Pipe &p, It it, const CUtensorMap *tm_x, const CU
                 uint8_t *a = p.stages + stage * p.stage_bytes;
                 ptx::mbar_arrive_expect_tx(&p.full[stage], p.stage_bytes);
                 // boxes past K read as zeros
-                ptx::tma_load_2d(a, tm_x, kb * kBK, sg.m * kBM, &p.full[stage], pol_x);
-                ptx::tma_load_2d(a + kBoxA, tm_w, kb * kBK, sg.n * NPAD, &p.full[stage], pol_w);
+                ptx::tma_load_2d(a, tm_x, kb * kKS, sg.m * kBM, &p.full[stage], pol_x);
+                ptx::tma_load_2d(a + kBoxA, tm_w, kb * kKS, sg.n * NPAD, &p.full[stage], pol_w);
                 issued_mask |= 1u << stage;
                 issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             }
@@ -205,10 +210,10 @@ __device__ void producer(const Pipe &p, It it, const CUtensorMap *tm_x, const CU
 }
 
 // ----------------------------------------------------------- MMA issuer
-template <int NPAD, typename It>
+template <int NPAD, typename It, bool kFp8 = false>
 __device__ void mma_issuer(const Pipe &p, It it)
 {
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, NPAD);
+    constexpr uint32_t idesc = kFp8 ? ptx::idesc_e4m3_f32(kBM, NPAD) : ptx::idesc_bf16_f32(kBM, NPAD);
     constexpr int kBoxA = kBoxABytes;
     int stage = 0;
     uint32_t phase = 0;
@@ -230,10 +235,14 @@ __device__ void mma_issuer(const Pipe &p, It it)
             const uint64_t a_desc = ptx::smem_desc_sw128(a_addr);
             const uint64_t b_desc = ptx::smem_desc_sw128(a_addr + kBoxA);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-                // advancing K by 16 bf16 = 32 bytes inside the swizzle row
-                ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
-                              (kb > sg.k0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk) {
+                // 32 bytes of K per instruction (16 bf16 or 32 e4m3): +2 in the
+                // descriptor's address field
+                const uint32_t accum = (kb > sg.k0 || kk > 0) ? 1u : 0u;
+                if constexpr (kFp8)
+                    ptx::mma_e4m3(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, accum);
+                else
+                    ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, accum);
             }
             ptx::mma_commit(&p.empty[stage]);  // frees the stage once these MMAs finish
             if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
@@ -253,7 +262,7 @@ __device__ void mma_issuer(const Pipe &p, It it)
 
 // ----------------------------------------------------------- square-sum
 // Warps w0..w0+3; thread `row` (0..127) sums row `row` of every stage.
-template <int NPAD, typename It>
+template <int NPAD, typename It, bool kFp8 = false>
 __device__ void square_sum(const Pipe &p, It it, int row, int lane)
 {
     int stage = 0;
@@ -274,13 +283,25 @@ __device__ void square_sum(const Pipe &p, It it, int row, int lane)
                 // 16-byte chunk j of the row lives at chunk (j ^ row%8) (128-byte
                 // swizzle); a row sum needs every chunk once, in any order.
                 const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
-                const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
-                const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
-                const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
-                ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
-                ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
-                ss0 = fmaf(a4, a4, ss0); ss1 = fmaf(a5, a5, ss1);
-                ss2 = fmaf(a6, a6, ss2); ss3 = fmaf(a7, a7, ss3);
+                if constexpr (kFp8) {
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        float a0, a1, a2, a3;
+                        e4m3x2_to_f32(w[h], a0, a1);
+                        e4m3x2_to_f32(w[h] >> 16, a2, a3);
+                        ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
+                        ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
+                    }
+                } else {
+                    const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
+                    const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
+                    const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
+                    ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
+                    ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
+                    ss0 = fmaf(a4, a4, ss0); ss1 = fmaf(a5, a5, ss1);
+                    ss2 = fmaf(a6, a6, ss2); ss3 = fmaf(a7, a7, ss3);
+                }
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&p.empty[stage]);

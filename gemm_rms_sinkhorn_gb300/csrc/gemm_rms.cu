@@ -60,7 +60,8 @@ struct KCfg {
 // kSplit: the weight operand holds every column twice, as the bf16 value
 // nearest the fp32 weight and the bf16 value nearest the remainder (rows 2k,
 // 2k+1 of φᵀ), and the epilogue adds each pair: Ỹ[k] = acc[2k] + acc[2k+1].
-template <int NPAD, bool kSplit>
+// kFp8: X and φᵀ are e4m3 codes (128 per 128-byte row, kind::f8f6f4 MMAs).
+template <int NPAD, bool kSplit, bool kFp8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
@@ -103,12 +104,12 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 
     if (warp == 0) {
         if (lane == 0)  // X streams through once: evict it first
-            pipe::producer<NPAD>(p, segs, &tm_x, &tm_w, ptx::policy_evict_first(),
-                                 cta == 0 ? stall_stage : -1);
+            pipe::producer<NPAD, SegIter, kFp8>(p, segs, &tm_x, &tm_w, ptx::policy_evict_first(),
+                                                cta == 0 ? stall_stage : -1);
     } else if (warp == 1) {
-        if (lane == 0) pipe::mma_issuer<NPAD>(p, segs);
+        if (lane == 0) pipe::mma_issuer<NPAD, SegIter, kFp8>(p, segs);
     } else if (warp < 6) {
-        pipe::square_sum<NPAD>(p, segs, (warp - 2) * 32 + lane, lane);
+        pipe::square_sum<NPAD, SegIter, kFp8>(p, segs, (warp - 2) * 32 + lane, lane);
     } else {
         // ----------------------------------------------- epilogue (warps 6..9)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -252,11 +253,11 @@ int npad_of(int n)
 // Grid: one CTA per SM, but no more than 32 contributors per token tile (the
 // last arriver's fixed-order sum grows with the fan-in) and at least one
 // stage of K per CTA.
-Sched make_sched(int64_t B, int n, int64_t C, int num_sms)
+Sched make_sched(int64_t B, int n, int64_t C, int num_sms, int k_per_block = kBK)
 {
     Sched s;
     s.m_tiles = static_cast<int>((B + kBM - 1) / kBM);
-    s.kbt = static_cast<int>((n * C + kBK - 1) / kBK);
+    s.kbt = static_cast<int>((n * C + k_per_block - 1) / k_per_block);
     s.total = static_cast<int64_t>(s.m_tiles) * s.kbt;
     int64_t g = num_sms;
     if (g > 32LL * s.m_tiles) g = 32LL * s.m_tiles;
@@ -282,7 +283,7 @@ struct LaunchArgs {
     int64_t stall_stage;
 };
 
-template <int NPAD, bool kSplit>
+template <int NPAD, bool kSplit, bool kFp8 = false>
 cudaError_t launch_cfg(const LaunchArgs &a)
 {
     using Cf = KCfg<NPAD>;
@@ -290,19 +291,29 @@ cudaError_t launch_cfg(const LaunchArgs &a)
     static std::mutex mu;
     if (a.device < 64 && !((configured >> a.device) & 1)) {
         std::lock_guard<std::mutex> lock(mu);
-        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD, kSplit>,
+        cudaError_t e = cudaFuncSetAttribute(gemm_rms_kernel<NPAD, kSplit, kFp8>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cf::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured |= 1ull << a.device;
     }
-    return launch_pdl(gemm_rms_kernel<NPAD, kSplit>, dim3(a.s.grid), dim3(kThreads),
+    return launch_pdl(gemm_rms_kernel<NPAD, kSplit, kFp8>, dim3(a.s.grid), dim3(kThreads),
                       Cf::kSmemBytes, a.stream, *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r,
                       a.tickets, a.partials, a.wait_limit_ns, a.stall_stage);
 }
 
-cudaError_t dispatch(int npad, bool split, const LaunchArgs &a)
+cudaError_t dispatch(int npad, bool split, bool fp8, const LaunchArgs &a)
 {
+    if (fp8) {
+        switch (npad) {
+        case 16: return launch_cfg<16, false, true>(a);
+        case 32: return launch_cfg<32, false, true>(a);
+        case 48: return launch_cfg<48, false, true>(a);
+        case 64: return launch_cfg<64, false, true>(a);
+        case 80: return launch_cfg<80, false, true>(a);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     if (split) {
         switch (npad) {  // 2N padded: n = 1, 2 -> 16; 3 -> 32; 4 -> 48; 5 -> 80; 6 -> 96; 7 -> 128; 8 -> 160
         case 16: return launch_cfg<16, true>(a);
@@ -367,18 +378,31 @@ static EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
-bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows)
+static bool make_tmap_2d(CUtensorMap *m, CUtensorMapDataType type, int esize, const void *base,
+                         uint64_t cols, uint64_t rows, uint32_t box_rows)
 {
     EncodeTiledFn f = encode_fn();
     if (!f) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(pipe::kBK), box_rows};
+    cuuint64_t strides[1] = {cols * static_cast<uint64_t>(esize)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};  // one 128-byte row
     cuuint32_t estr[2] = {1, 1};
-    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
-             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+    return f(m, type, 2, const_cast<void *>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D bf16 tensor [rows][cols] (cols contiguous), box [box_rows][64], 128-byte swizzle.
+bool make_tmap(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint32_t box_rows)
+{
+    return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, cols, rows, box_rows);
+}
+
+// The same for e4m3 codes: box [box_rows][128].
+static bool make_tmap_e4m3(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                           uint32_t box_rows)
+{
+    return make_tmap_2d(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, base, cols, rows, box_rows);
 }
 
 size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
@@ -390,20 +414,21 @@ size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
     return tickets_bytes(s.m_tiles) + slots * kBM * (N + 1) * sizeof(float);
 }
 
-static cudaError_t launch_gemm_rms_impl(const uint16_t *X, const uint16_t *phi_t, int64_t B,
-                                        int n, int64_t C, float *Y, float *r, void *workspace,
+static cudaError_t launch_gemm_rms_impl(const void *X, const void *phi_t, int64_t B, int n,
+                                        int64_t C, float *Y, float *r, void *workspace,
                                         int num_sms, cudaStream_t stream, uint64_t wait_limit_ns,
-                                        int64_t stall_stage, bool split)
+                                        int64_t stall_stage, bool split, bool fp8)
 {
     const int N = num_coeffs(n);
     const int64_t K = n * C;
-    const Sched s = make_sched(B, n, C, num_sms);
+    const Sched s = make_sched(B, n, C, num_sms, fp8 ? 2 * kBK : kBK);
     CUtensorMap tx, tw;
     const int wrows = split ? 2 * N : N;  // rows of the weight operand
     const int npad = (wrows + 15) / 16 * 16;
-    if (!make_tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
-        !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(wrows),
-                   static_cast<uint32_t>(npad)))
+    const auto tmap = fp8 ? make_tmap_e4m3 : make_tmap;
+    if (!tmap(&tx, X, static_cast<uint64_t>(K), static_cast<uint64_t>(B), kBM) ||
+        !tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(wrows),
+              static_cast<uint32_t>(npad)))
         return cudaErrorInvalidValue;
     int *tickets = static_cast<int *>(workspace);
     float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) +
@@ -416,7 +441,7 @@ static cudaError_t launch_gemm_rms_impl(const uint16_t *X, const uint16_t *phi_t
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     const LaunchArgs a{&tx, &tw, B, N, static_cast<int>(K), s, Y, r, tickets, partials, stream,
                        device, wait_limit_ns, stall_stage};
-    return dispatch(npad, split, a);
+    return dispatch(npad, split, fp8, a);
 }
 
 cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
@@ -424,7 +449,7 @@ cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B,
                             cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
 {
     return launch_gemm_rms_impl(X, phi_t, B, n, C, Y, r, workspace, num_sms, stream,
-                                wait_limit_ns, stall_stage, false);
+                                wait_limit_ns, stall_stage, false, false);
 }
 
 cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, int64_t B, int n,
@@ -432,7 +457,15 @@ cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, 
                                   cudaStream_t stream)
 {
     return launch_gemm_rms_impl(X, phi_split, B, n, C, Y, r, workspace, num_sms, stream,
-                                kWaitLimitNs, -1, true);
+                                kWaitLimitNs, -1, true, false);
+}
+
+cudaError_t launch_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n,
+                                 int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                                 cudaStream_t stream)
+{
+    return launch_gemm_rms_impl(X, phi_t, B, n, C, Y, r, workspace, num_sms, stream,
+                                kWaitLimitNs, -1, false, true);
 }
 
 cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,

@@ -82,6 +82,11 @@ cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, 
                                   cudaStream_t stream);
 cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,
                              cudaStream_t stream);
+// The fp8 form: X [B][K] and phi_t [N][K] as e4m3 codes (kind::f8f6f4 MMAs,
+// 128 K values per stage); the same Y, r and workspace.
+cudaError_t launch_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n,
+                                 int64_t C, float *Y, float *r, void *workspace, int num_sms,
+                                 cudaStream_t stream);
 
 // Tensor map of a 2-D bf16 tensor [rows][cols] (cols contiguous): boxes of
 // box_rows × 64 elements, 128-byte swizzle, zero fill out of bounds.
@@ -142,6 +147,13 @@ cudaError_t run_forward_host(const uint16_t *X, const uint16_t *phi_t, const uin
                              int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
                              float *H_post, float *H_res, uint16_t *F_pre, uint16_t *X_next,
                              void *scratch, int num_sms, cudaStream_t stream);
+
+// ---- step 4 on e4m3 activations (apply_e4m3.cu); C % 16 == 0
+cudaError_t launch_pre_apply_e4m3(const uint8_t *X, const float *H_pre, int64_t B, int n,
+                                  int64_t C, uint8_t *F_pre, cudaStream_t stream);
+cudaError_t launch_post_res_apply_e4m3(const uint8_t *X, const uint8_t *F_out, const float *H_res,
+                                       const float *H_post, int64_t B, int n, int64_t C,
+                                       uint8_t *X_next, cudaStream_t stream);
 
 // ---- C = rmsnorm(A) @ B, Lazy Pre-Norm (rmsnorm_gemm.cu)
 size_t rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N, int num_sms);

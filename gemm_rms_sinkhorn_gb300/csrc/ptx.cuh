@@ -222,6 +222,26 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Instruction descriptor, kind::f8f6f4: fp32 accumulator, e4m3 A and B (format
+// code 0 in both fields), both K-major, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N)
+{
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (+)= A·B with 8-bit operands, K = 32 per instruction.
+__device__ __forceinline__ void mma_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // ------------------------------------------ programmatic dependent launch
 
 // Acquire load of a global 32-bit word at GPU scope: writes that another CTA
@@ -271,6 +291,25 @@ __device__ __forceinline__ void st_stream_v4(void *p, uint4 v)
 
 // bf16 <-> fp32 on packed pairs.  Widening is exact (bf16 is the top half of
 // binary32); narrowing rounds to nearest even.
+// Two e4m3 codes (bits 0-7 and 8-15 of w) to fp32: exact (e4m3 is a subset of f16).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t w, float &lo, float &hi)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w & 0xFFFFu)));
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi) : "r"(h2));
+}
+
+// Two fp32 to e4m3 codes (lo in bits 0-7): round to nearest even, saturating
+// finite values to ±448.
+__device__ __forceinline__ uint32_t f32x2_to_e4m3(float lo, float hi)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

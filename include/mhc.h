@@ -17,6 +17,7 @@
  *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
  *   mhc_rmsnorm_gemm    C = rmsnorm(A) @ B for any N (Lazy Pre-Norm, second page §2)
  *   mhc_*_f32w / _split / _f32   the fp32-weight, fp32-F_out precision variant (§5)
+ *   mhc_*_e4m3          the fp8 e4m3 precision variant (§4)
  *
  * Shapes: B tokens (batch × sequence), expansion n, hidden size C,
  * K = n·C, N = n² + 2n.
@@ -225,6 +226,32 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
                      float alpha_pre, float alpha_post, float alpha_res, const float *bias,
                      int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
                      float *H_post, float *H_res, mhc_bf16 *F_pre, mhc_bf16 *X_next,
+                     void *workspace, size_t workspace_bytes, mhc_stream_t stream);
+
+/*
+ * fp8 e4m3 precision variant (the precision of the page's first benchmark,
+ * §4): X [B][K], φᵀ [N][K], F_out, F_pre [B][C] and X_next [B][K] are e4m3
+ * codes (OCP E4M3: bias 7, 3 mantissa bits, largest finite 448, no
+ * infinities), one byte each; Y, r, b and H stay fp32.  The GEMM runs
+ * tcgen05 kind::f8f6f4 (e4m3 × e4m3, fp32 accumulate) on 128-value K stages;
+ * the square sum decodes the same tiles; the apply kernels decode exactly,
+ * mix in fp32 and round the outputs to nearest even, saturating to ±448.
+ * Rules of the bf16 calls, plus C % 16 == 0 (MHC_ERR_UNSUPPORTED otherwise);
+ * the workspace is mhc_workspace_bytes(B, n, C).  mhc_forward_e4m3 always runs
+ * the four-kernel chain.
+ */
+int mhc_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n, int64_t C,
+                      float *Y, float *r, void *workspace, size_t workspace_bytes,
+                      mhc_stream_t stream);
+int mhc_pre_apply_e4m3(const uint8_t *X, const float *H_pre, int64_t B, int n, int64_t C,
+                       uint8_t *F_pre, mhc_stream_t stream);
+int mhc_post_res_apply_e4m3(const uint8_t *X, const uint8_t *F_out, const float *H_res,
+                            const float *H_post, int64_t B, int n, int64_t C, uint8_t *X_next,
+                            mhc_stream_t stream);
+int mhc_forward_e4m3(const uint8_t *X, const uint8_t *phi_t, const uint8_t *F_out,
+                     float alpha_pre, float alpha_post, float alpha_res, const float *bias,
+                     int iters, int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                     float *H_post, float *H_res, uint8_t *F_pre, uint8_t *X_next,
                      void *workspace, size_t workspace_bytes, mhc_stream_t stream);
 
 /*

@@ -204,3 +204,11 @@ def test_rmsnorm_gemm_validates_on_the_host():
     assert f(A + 8, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_ALIGN
     assert f(A, B_, 16, 64, 64, 1e-5, A + 64, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
     assert mhc._lib.mhc_rmsnorm_gemm_workspace_bytes(16, 64, 64) == 0  # needs a device
+
+
+def test_e4m3_calls_validate_on_the_host():
+    assert L.mhc_pre_apply_e4m3(A, B_, 4, 4, 24, C_, None) == mhc.MHC_ERR_UNSUPPORTED  # C % 16
+    assert L.mhc_pre_apply_e4m3(A, B_, 4, 4, 32, C_, None) == NO_DEVICE
+    assert L.mhc_gemm_rms_e4m3(A, B_, 4, 4, 32, C_, D, W, 1 << 30, None) == NO_DEVICE
+    assert L.mhc_post_res_apply_e4m3(A, B_, C_, D, 4, 4, 32, A, None) == NO_DEVICE  # in place
+    assert L.mhc_post_res_apply_e4m3(A, B_, C_, D, 4, 4, 32, A + 16, None) == mhc.MHC_ERR_INVALID
