@@ -54,8 +54,11 @@ def algorithmic_bytes(B: int, n: int, C: int, precision: str = "bf16") -> dict:
     H = 4 * B * (2 * n + n * n)
     wrows = 2 * N if precision == "f32w" else N
     f_in = 4 * B * C if precision == "f32w" else Fc
+    wbytes = 2 * wrows * K
+    if precision == "e4m3":  # one byte per activation and weight value
+        X, Fc, f_in, wbytes = B * K, B * C, B * C, N * K
     return {
-        "gemm_rms": X + 2 * wrows * K + 4 * B * N + 4 * B,
+        "gemm_rms": X + wbytes + 4 * B * N + 4 * B,
         "coeffs": 4 * B * N + 4 * B + 4 * N + H,
         "pre_apply": X + 4 * B * n + Fc,
         "post_res_apply": X + f_in + 4 * B * n * n + 4 * B * n + X,
@@ -427,9 +430,10 @@ def main() -> int:
                          "forced through its test hook: chain (four kernels), decode (the "
                          "small-batch one-launch steps 1-4a), fused (the large-batch one-kernel "
                          "steps 1-4a)")
-    ap.add_argument("--precision", default="bf16", choices=["bf16", "f32w"],
+    ap.add_argument("--precision", default="bf16", choices=["bf16", "f32w", "e4m3"],
                     help="latency mode: f32w times mhc_forward_f32w (fp32 weight as split bf16 "
-                         "pairs, fp32 F_out) instead of the bf16 forward")
+                         "pairs, fp32 F_out), e4m3 times mhc_forward_e4m3 (fp8 activations "
+                         "and weight), instead of the bf16 forward")
     ap.add_argument("--tokens", type=int, default=None,
                     help="latency mode: the workload with this many tokens instead")
     ap.add_argument("--mode", default="full",
@@ -497,6 +501,16 @@ def main() -> int:
         mhc.mhc_split_phi(phi32, n, C, phi_t)
         F_out = torch.from_numpy(synth.normal_f32((B, C), rank, 1, wl.fout_std)).to(dev)
         forward_call = mhc.mhc_forward_f32w
+    elif args.precision == "e4m3":
+        if args.mode != "latency":
+            ap.error("--precision e4m3 only applies to --mode latency")
+        to8 = lambda a: torch.from_numpy(a).to(dev)
+        X = to8(synth.normal_e4m3((B, wl.K), rank, 0, 1.0))
+        phi_t = to8(synth.normal_e4m3((wl.N, wl.K), rank, 2, wl.phi_std))
+        F_out = to8(synth.normal_e4m3((B, C), rank, 1, wl.fout_std))
+        out["F_pre"] = torch.empty(B, C, dtype=torch.uint8, device=dev)
+        out["X_next"] = torch.empty(B, wl.K, dtype=torch.uint8, device=dev)
+        forward_call = mhc.mhc_forward_e4m3
 
     def step(on_stream=None):
         forward_call(X, phi_t, F_out, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,

@@ -310,6 +310,35 @@ __device__ __forceinline__ uint32_t f32x2_to_e4m3(float lo, float hi)
     return r;
 }
 
+// Two e4m3 codes (bits 0-7, 8-15) to an f16x2 (exact), and back: f16x2 to two
+// e4m3 codes, round to nearest even, saturating to ±448.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t w)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w & 0xFFFFu)));
+    return h2;
+}
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t h2)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(h2));
+    return r;
+}
+// d = a·b + c on f16x2, and an f16x2 holding (v, v) from an fp32.
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c)
+{
+    uint32_t d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+__device__ __forceinline__ uint32_t f16x2_splat(float v)
+{
+    uint32_t d;
+    asm("{\n\t.reg .f16 h;\n\tcvt.rn.f16.f32 h, %1;\n\tmov.b32 %0, {h, h};\n\t}"
+        : "=r"(d) : "f"(v));
+    return d;
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

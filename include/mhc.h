@@ -235,7 +235,9 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
  * infinities), one byte each; Y, r, b and H stay fp32.  The GEMM runs
  * tcgen05 kind::f8f6f4 (e4m3 × e4m3, fp32 accumulate) on 128-value K stages;
  * the square sum decodes the same tiles; the apply kernels decode exactly,
- * mix in fp32 and round the outputs to nearest even, saturating to ±448.
+ * mix in f16 (2^-11 rounding, well below e4m3's 2^-4; partial sums beyond
+ * ±65504, possible only for an unnormalised H_res, saturate) and round the
+ * outputs to nearest even, saturating to ±448.
  * Rules of the bf16 calls, plus C % 16 == 0 (MHC_ERR_UNSUPPORTED otherwise);
  * the workspace is mhc_workspace_bytes(B, n, C).  mhc_forward_e4m3 always runs
  * the four-kernel chain.
