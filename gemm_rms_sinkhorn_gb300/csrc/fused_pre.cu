@@ -7,27 +7,31 @@
 //   H_pre, H_post, H_res = coefficients(Y,r)  (S2, S3)
 //   F_pre = Σ_i H_pre[i]·X[i]                 (S4a)
 //
-// The batch is walked in chunks of CH token tiles (128 tokens each), small
-// enough for the chunk's X to stay in L2.  Every CTA works on every chunk:
-// the G = CH·P CTAs are P "contributors" per tile, and contributor p of a
-// tile takes K blocks [kbt·p/P, kbt·(p+1)/P) of it through the TMA → tcgen05
-// pipeline of gemm_pipeline.cuh (X loaded with the evict_normal L2 policy).
-// Per chunk and CTA, sixteen warps share the work:
-//   warps 0-5   the pipeline: TMA, MMA, square-sum;
-//   warps 6-9   epilogue: park this CTA's partial (row sums of Y and Σx²),
-//               wait (bounded) for the P partials of its tile, then finish its
-//               own rows [128·p/P, 128·(p+1)/P): the sum of the P partials in
-//               contributor order (deterministic), then Y and r;
-//   warp 15     loader: once a tile's partials are all in (its X has just
-//               streamed through L2), bulk-copies the CTA's rows of X, piece by
-//               piece, into a ring of shared-memory slots;
-//   warps 10-13 pre-apply: H_pre of the rows (σ only), then F_pre of each
-//               piece from shared memory;
+// The batch is walked in chunks of CH token tiles (128 tokens each).  Every
+// CTA works on every chunk: the G = CH·P CTAs are P "contributors" per tile,
+// and contributor p of a tile takes K blocks [kbt·p/P, kbt·(p+1)/P) of it
+// through the TMA → tcgen05 pipeline of gemm_pipeline.cuh (X loaded with the
+// evict_normal L2 policy), parks its partial row sums in global memory and
+// later finishes its own rows [128·p/P, 128·(p+1)/P) of the tile: the fixed-
+// order sum of the P partials, Y and r, the coefficients, and F_pre from a
+// second read of those rows' X.  That read hits L2 because the producer is
+// held back (LeadIter) until at most `lead` chunks of X have been streamed
+// and not yet re-read.  Sixteen warps per CTA:
+//   warps 0-5   the pipeline: TMA (throttled), MMA, square-sum;
+//   warps 6-9   epilogue: park this CTA's partial of each tile (row sums of Y
+//               and Σx²), count it in the tile's ticket, then finish the rows
+//               of the tile before (whose partials have had a segment's time
+//               to arrive): the fixed-order sum of its P partials, all loads
+//               issued at once, then Y and r;
+//   warps 10-13 finisher: H_pre of the finished rows (σ only), then F_pre of
+//               each piece from shared memory;
 //   warp 14     coefficients: H_pre, H_post and the Sinkhorn–Knopp H_res of
-//               the rows (token_coeffs, as the standalone kernel), off the
-//               critical path.
-// Partial slots alternate between two buffers by chunk parity; before reusing
-// one a CTA waits (bounded) until the readers of two chunks back are done.
+//               the rows (token_coeffs, as the standalone kernel);
+//   warp 15     loader: once the tile's P partials are in (its X has just
+//               streamed through L2), bulk-copies the CTA's rows of X, piece
+//               by piece, into a ring of shared-memory slots.
+// Partials rotate through nb buffers by chunk; before reusing one a CTA waits
+// (bounded) until the P finishers of that buffer's previous tile have read it.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -51,10 +55,16 @@ constexpr int kEpiT = 128;
 constexpr int kPreT = 128;
 constexpr int kMaxRows = 16;    // rows each contributor finishes per tile (P >= 8)
 constexpr int kRowBufs = 4;     // finished-row buffers in flight
-constexpr int kSlots = 8;       // pre-apply X slots
-constexpr int kSlotBytes = 8192;
-constexpr int kReduceBatch = 8; // partials in flight per output of the fixed-order sum
-constexpr int64_t kChunkBytes = 40LL << 20;  // X bytes per chunk, kept in L2
+constexpr int kSlotBytes = 8192;  // one piece of the X re-read
+constexpr int kReduceBatch = 40;  // partials in flight per thread of the fixed-order sums
+// X bytes per chunk and chunks streamed ahead of the re-read (see LeadIter,
+// >= 2).  Measured at B=16384, n=4, C=7168: 4-tile chunks (29 MB) with lead 3
+// were fastest, though about a third of the re-read then misses L2; 2-tile
+// chunks keep it in L2 but pay the per-tile latencies twice as often.
+constexpr int64_t kChunkBytes = 32LL << 20;
+constexpr int kLeadChunks = 3;
+constexpr int kMaxPartBufs = 8;
+static_assert(kLeadChunks >= 2, "see LeadIter");
 
 __device__ int g_fused_status;
 
@@ -63,6 +73,11 @@ struct FCfg {
     static constexpr int N = n * n + 2 * n;
     static constexpr int NPAD = (N + 15) / 16 * 16;
     static constexpr int kRingBudget = n <= 4 ? 124 * 1024 : 134 * 1024;
+    static constexpr int kSlots = n <= 4 ? 10 : 8;  // X re-read slots (shared memory left over)
+    // n <= 4: the epilogue stages its partial in shared memory and stores it
+    // coalesced; wider rows do not fit and are stored from registers
+    static constexpr bool kStage = n <= 4;
+    static constexpr int kStageBytes = kStage ? kBM * (N + 1) * 4 : 0;
     using C = pipe::Cfg<NPAD, kRingBudget>;
     // channels per piece: one pass of the 128 pre-apply threads (8 each), n streams per slot
     static constexpr int kW = (kSlotBytes / (2 * n)) / 8 * 8 < 8 * kPreT
@@ -70,16 +85,21 @@ struct FCfg {
                                   : 8 * kPreT;
     static constexpr int kRowsBytes = kRowBufs * kMaxRows * (N + 1) * 4;
     static constexpr int kHpBytes = kMaxRows * 8 * 4;
-    static constexpr int kOwnBarBytes = 256;                         // barriers of this kernel
+    static constexpr int kRedBytes = kPreT * 4;                      // group sums of the reduction
+    static constexpr int kOwnBarBytes = 384;                         // barriers of this kernel
     static constexpr int kSmemBytes = 1024 + C::kRingBytes + pipe::kSsBytes + pipe::kBarrierBytes +
-                                      kSlots * kSlotBytes + kRowsBytes + kHpBytes + kOwnBarBytes;
+                                      kSlots * kSlotBytes + kRowsBytes + kHpBytes + kRedBytes +
+                                      kStageBytes + kOwnBarBytes;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     static_assert(kW % 8 == 0 && kW / 8 <= kPreT, "a piece is one pass of the pre-apply warps");
-    static_assert((2 + 2 * kRowBufs + 2 * kSlots) * 8 <= kOwnBarBytes, "barrier area");
+    static_assert((2 + 2 * kRowBufs + 2 * kSlots) * 8 + 4 <= kOwnBarBytes, "barrier area");
+    static_assert(!kStage || (32 * (N + 1)) % 4 == 0, "a warp's staged rows are whole float4s");
 };
 
 struct FSched {
     int m_tiles, kbt, CH, P, nchunks;
+    int lead;  // chunks the GEMM may run ahead of this CTA's finished pre-apply
+    int nb;    // partial buffers, used in turn by consecutive chunks
 };
 
 // The segments of the CTA in tile slot j, contributor p: one per chunk.
@@ -97,6 +117,38 @@ struct ChunkIter {
             return true;
         }
         return false;
+    }
+};
+
+// The producer's segments, each released only once the pre-apply warps of
+// this CTA have finished the segment `lead` places back: the X streamed for
+// the GEMM but not yet re-read stays within `lead` chunks, which is what has
+// to fit in L2.  lead >= 2: the epilogue finishes a tile's rows after parking
+// the next tile, so with lead = 1 a segment would wait for its own park.  On a
+// timeout or an abort the segment is still returned; the producer's next
+// stage wait then sees the abort and drains its copies.
+struct LeadIter {
+    ChunkIter it;
+    const volatile int *pre_done;  // segments the pre-apply warps have finished
+    const pipe::Pipe *p;
+    int seg;
+    __device__ bool next(Segment &sg) {
+        if (!it.next(sg)) return false;
+        const int need = seg + 1 - it.s.lead;
+        ++seg;
+        if (need <= 0) return true;
+        const uint64_t t0 = ptx::globaltimer_ns();
+        for (uint32_t polls = 0; *pre_done < need; ++polls) {
+            if ((polls & 63) == 63) {
+                if (*p->abort) return true;
+                if (ptx::globaltimer_ns() - t0 > p->limit_ns) {
+                    pipe::raise_timeout(*p);
+                    return true;
+                }
+            }
+            __nanosleep(32);
+        }
+        return true;
     }
 };
 
@@ -125,6 +177,22 @@ __device__ __forceinline__ int clamp_rows(int r0, int r1, int valid)
     return hi > r0 ? hi - r0 : 0;
 }
 
+// Σ over contributors q in [q0, q1) of src[q·qs], in order, kReduceBatch loads
+// in flight at a time (s + 0 is exact for the padding).
+__device__ __forceinline__ float partial_sum(const float *src, int64_t qs, int q0, int q1)
+{
+    float s = 0.f;
+    for (int q = q0; q < q1; q += kReduceBatch) {
+        float vb[kReduceBatch];
+#pragma unroll
+        for (int u = 0; u < kReduceBatch; ++u)
+            vb[u] = q + u < q1 ? __ldcg(src + static_cast<int64_t>(q + u) * qs) : 0.f;
+#pragma unroll
+        for (int u = 0; u < kReduceBatch; ++u) s += vb[u];
+    }
+    return s;
+}
+
 template <int n>
 __global__ void __launch_bounds__(kThreads, 1)
 fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
@@ -138,8 +206,9 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     using F = FCfg<n>;
     constexpr int N = F::N;
     constexpr int NPAD = F::NPAD;
-    constexpr int stride = N + 1;  // a partial row: N sums of Y, then Σx²
+    constexpr int stride = N + 1;  // a finished row: N sums of Y, then r
     constexpr int W = F::kW;
+    constexpr int kSlots = F::kSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -148,12 +217,15 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     uint8_t *slots = after;                                             // [kSlots][kSlotBytes]
     float *rows_buf = reinterpret_cast<float *>(slots + kSlots * kSlotBytes);  // [kRowBufs][kMaxRows][stride]
     float *hp_buf = rows_buf + kRowBufs * kMaxRows * stride;            // [kMaxRows][8]
-    uint64_t *epi_bar = reinterpret_cast<uint64_t *>(hp_buf + kMaxRows * 8);
+    float *red = hp_buf + kMaxRows * 8;                                 // [kEpiT]
+    float *stage = red + kEpiT;                                         // [kBM][stride] if F::kStage
+    uint64_t *epi_bar = reinterpret_cast<uint64_t *>(stage + F::kStageBytes / 4);
     uint64_t *pre_bar = epi_bar + 1;
-    uint64_t *rows_full = pre_bar + 1;            // [kRowBufs] epilogue -> loader, pre, coefficients
-    uint64_t *rows_empty = rows_full + kRowBufs;  // [kRowBufs] pre + coefficients -> epilogue
-    uint64_t *slot_full = rows_empty + kRowBufs;  // [kSlots] loader -> pre
-    uint64_t *slot_empty = slot_full + kSlots;    // [kSlots] pre -> loader
+    uint64_t *rows_full = pre_bar + 1;            // [kRowBufs] epilogue -> finisher, coefficients
+    uint64_t *rows_empty = rows_full + kRowBufs;  // [kRowBufs] finisher, coefficients -> epilogue
+    uint64_t *slot_full = rows_empty + kRowBufs;  // [kSlots] loader -> finisher
+    uint64_t *slot_empty = slot_full + kSlots;    // [kSlots] finisher -> loader
+    volatile int *pre_done = reinterpret_cast<volatile int *>(slot_empty + kSlots);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -161,19 +233,22 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     const int j = g / fs.P, pc = g - (g / fs.P) * fs.P;  // tile slot, contributor
     const int G = fs.CH * fs.P;
     const int r0 = kBM * pc / fs.P, r1 = kBM * (pc + 1) / fs.P;  // rows this CTA finishes
+    // one CTA's partial: [kBM][N + 1] (N sums of Y, then Σx²)
+    const int64_t part_stride = static_cast<int64_t>(kBM) * stride;
 
     if (threadIdx.x == 0) {
         pipe::init_barriers(p);
         ptx::mbar_init(epi_bar, kEpiT);
         ptx::mbar_init(pre_bar, kPreT);
         for (int a = 0; a < kRowBufs; ++a) {
-            ptx::mbar_init(&rows_full[a], 4);
-            ptx::mbar_init(&rows_empty[a], 4 + 1);  // pre warps + the coefficient warp
+            ptx::mbar_init(&rows_full[a], 1);
+            ptx::mbar_init(&rows_empty[a], 2);  // finisher + coefficient warp
         }
         for (int a = 0; a < kSlots; ++a) {
             ptx::mbar_init(&slot_full[a], 1);
             ptx::mbar_init(&slot_empty[a], 4);
         }
+        *pre_done = 0;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -191,7 +266,8 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
 
     if (warp == 0) {
         if (lane == 0)  // X stays in L2 until the loader re-reads it
-            pipe::producer<NPAD>(p, segs, &tm_x, &tm_w, ptx::policy_evict_normal(), -1);
+            pipe::producer<NPAD>(p, LeadIter{segs, pre_done, &p, 0}, &tm_x, &tm_w,
+                                 ptx::policy_evict_normal(), -1);
     } else if (warp == 1) {
         if (lane == 0) pipe::mma_issuer<NPAD>(p, segs);
     } else if (warp < 6) {
@@ -202,72 +278,122 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
         const int row = q * 32 + lane;
         const int et = threadIdx.x - 192;
         uint32_t epi_phase = 0;
-        int seg = 0;
+
+        // Finishes rows [r0, r0 + nrows) of the tile of segment fseg: item
+        // e = row·stride + column, summed over the P partials in contributor
+        // order (with few items the contributors are split into `groups`
+        // ranges whose sums are added in range order); then Y, r and the row
+        // buffer for the finisher and the coefficient warp.
+        auto finish = [&](int fseg, int t) -> bool {
+            const int c = t / fs.CH;
+            const int64_t row0 = static_cast<int64_t>(t) * kBM;
+            const int valid = static_cast<int>(B - row0 < kBM ? B - row0 : kBM);
+            const int nrows = clamp_rows(r0, r1, valid);
+            const int rb = fseg % kRowBufs;
+            float *rows = rows_buf + rb * kMaxRows * stride;
+            if (!pipe::wait(p, &rows_empty[rb], ((fseg / kRowBufs) & 1) ^ 1)) return false;
+            if (et == 0) wait_count(p, &tickets[t], fs.P);
+            // the acquire above and the group barrier order the partial loads
+            if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) return false;
+            const int E = nrows * stride;
+            const float *base =
+                partials + (static_cast<int64_t>(c % fs.nb) * G + static_cast<int64_t>(j) * fs.P) *
+                               part_stride + static_cast<int64_t>(r0) * stride;
+            auto emit = [&](int e, float s) {
+                const int rr = e / stride, cc = e - (e / stride) * stride;
+                const float out = cc < N ? s : sqrtf(s / static_cast<float>(K));
+                if (cc < N)
+                    Y[(row0 + r0 + rr) * N + cc] = out;
+                else
+                    r[row0 + r0 + rr] = out;
+                rows[rr * stride + cc] = out;
+            };
+            const int groups = E >= kEpiT || E == 0 ? 1 : kEpiT / E;
+            if (groups == 1) {
+                for (int e = et; e < E; e += kEpiT) emit(e, partial_sum(base + e, part_stride, 0, fs.P));
+            } else {
+                const int gi = et / E, e = et - (et / E) * E;
+                if (gi < groups)
+                    red[gi * E + e] = partial_sum(base + e, part_stride, fs.P * gi / groups,
+                                                  fs.P * (gi + 1) / groups);
+                if (!pipe::group_sync(p, epi_bar, epi_phase)) return false;
+                if (et < E) {
+                    float s = red[et];
+                    for (int g2 = 1; g2 < groups; ++g2) s += red[g2 * E + et];
+                    emit(et, s);
+                }
+            }
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) return false;
+            if (et == 0) {
+                atomicAdd(&done[t], 1);  // this CTA has read the tile's partials
+                ptx::mbar_arrive(&rows_full[rb]);
+            }
+            return true;
+        };
+
+        // Park each tile's partial, then finish the previous tile, whose
+        // partials have had a segment's time to arrive.
+        int seg = 0, prev_t = -1;
+        bool ok = true;
         ChunkIter it = segs;
         Segment sg;
         while (it.next(sg)) {
             float v[NPAD];
             float ss;
-            if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
+            if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) {
+                ok = false;
+                break;
+            }
             const int t = sg.m;
             const int c = t / fs.CH;
             const int64_t row0 = static_cast<int64_t>(t) * kBM;
             const int valid = static_cast<int>(B - row0 < kBM ? B - row0 : kBM);
 
-            // this slot was last read for tile t - 2·CH: wait for its P readers
-            if (c >= 2 && et == 0) wait_count(p, &done[t - 2 * fs.CH], fs.P);
-            if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) break;
-            float *mine = partials + (static_cast<int64_t>(c & 1) * G + g) * kBM * stride;
-            if (row < valid) {
+            // this buffer was last used for tile t - nb·CH: wait for its P readers
+            if (c >= fs.nb && et == 0) wait_count(p, &done[t - fs.nb * fs.CH], fs.P);
+            if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) {
+                ok = false;
+                break;
+            }
+            float *mine = partials + (static_cast<int64_t>(c % fs.nb) * G + g) * part_stride;
+            if constexpr (F::kStage) {
+                // this warp's 32 rows through shared memory, then 16-byte stores
+                // of the contiguous block (rows past the batch hold zeros and
+                // are never read)
+                float *st = stage + q * 32 * stride;
+#pragma unroll
+                for (int k = 0; k < NPAD; ++k)
+                    if (k < N) st[lane * stride + k] = v[k];
+                st[lane * stride + N] = ss;
+                __syncwarp();
+                const float4 *src4 = reinterpret_cast<const float4 *>(st);
+                float4 *dst4 = reinterpret_cast<float4 *>(mine + q * 32 * stride);
+                for (int f = lane; f < 32 * stride / 4; f += 32) __stcg(dst4 + f, src4[f]);
+                __syncwarp();
+            } else if (row < valid) {
 #pragma unroll
                 for (int k = 0; k < NPAD; ++k)
                     if (k < N) mine[row * stride + k] = v[k];
                 mine[row * stride + N] = ss;
             }
-            __threadfence();
-            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
-            if (et == 0) {
+            if (!pipe::group_sync(p, epi_bar, epi_phase)) {
+                ok = false;
+                break;
+            }
+            if (et == 0) {  // release: the group's stores, then the ticket
+                __threadfence();
                 atomicAdd(&tickets[t], 1);
-                wait_count(p, &tickets[t], fs.P);
             }
-            if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) break;
-            __threadfence();
-
-            // finish rows [r0, r1) of tile t: fixed-order sum of the P partials
-            const int rb = seg % kRowBufs;
-            if (!pipe::wait(p, &rows_empty[rb], ((seg / kRowBufs) & 1) ^ 1)) break;
-            const int nrows = clamp_rows(r0, r1, valid);
-            const int items = nrows * stride;
-            const float *base =
-                partials + (static_cast<int64_t>(c & 1) * G + static_cast<int64_t>(j) * fs.P) *
-                               kBM * stride;
-            const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
-            for (int i = et; i < items; i += kEpiT) {
-                const int rr = r0 + i / stride, cc = i - (i / stride) * stride;
-                const float *src = base + rr * stride + cc;
-                float s = 0.f;
-                for (int q0 = 0; q0 < fs.P; q0 += kReduceBatch) {
-                    float vb[kReduceBatch];
-#pragma unroll
-                    for (int u = 0; u < kReduceBatch; ++u)
-                        vb[u] = q0 + u < fs.P ? __ldcg(src + (q0 + u) * slot_stride) : 0.f;
-#pragma unroll
-                    for (int u = 0; u < kReduceBatch; ++u) s += vb[u];  // acc + 0 is exact
-                }
-                const float out = cc < N ? s : sqrtf(s / static_cast<float>(K));
-                if (cc < N)
-                    Y[(row0 + rr) * N + cc] = out;
-                else
-                    r[row0 + rr] = out;
-                rows_buf[(rb * kMaxRows + (rr - r0)) * stride + cc] = out;
+            if (seg > 0 && !finish(seg - 1, prev_t)) {
+                ok = false;
+                break;
             }
-            if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
-            if (et == 0) atomicAdd(&done[t], 1);  // this CTA has read the tile's partials
-            if (lane == 0) ptx::mbar_arrive(&rows_full[rb]);
+            prev_t = t;
             ++seg;
         }
+        if (ok && seg > 0) finish(seg - 1, prev_t);
     } else if (warp < 14) {
-        // ---------------------------------------- pre-apply (warps 10..13)
+        // ----------------------------------------- finisher (warps 10..13)
         const int pt = threadIdx.x - 320;
         uint32_t pre_phase = 0;
         int slot = 0;
@@ -290,7 +416,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                 hp_buf[tk * 8 + i] = pre_coeff(yrow[i], 1.0f / yrow[N], a_pre, bias[i]);
             }
             if (!pipe::group_sync(p, pre_bar, pre_phase)) break;
-            if (lane == 0) ptx::mbar_arrive(&rows_empty[rb]);
+            if (pt == 0) ptx::mbar_arrive(&rows_empty[rb]);
             // F_pre of each piece, in the loader's order
             for (int tk = 0; tk < nrows && ok; ++tk) {
                 float h[n];
@@ -318,6 +444,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             }
             if (!ok || !pipe::group_sync(p, pre_bar, pre_phase)) break;  // hp_buf is reused
             ++seg;
+            if (pt == 0) *pre_done = seg;  // this segment's X has been re-read
         }
     } else if (warp == 14) {
         // ------------------------------------- coefficients (warp 14)
@@ -345,11 +472,10 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     } else if (lane == 0) {
         // ------------------------------------------------ loader (warp 15)
         // X of a tile is in L2 once all its contributors have parked their
-        // partials, which the epilogue's rows_full signal follows.
+        // partials, which the tile's ticket counts.
         const uint64_t pol = ptx::policy_evict_first();  // the last read of this X
         int slot = 0;
         uint32_t slot_phase = 0;
-        int seg = 0;
         ChunkIter it = segs;
         Segment sg;
         bool ok = true;
@@ -358,7 +484,10 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int64_t row0 = static_cast<int64_t>(t) * kBM;
             const int valid = static_cast<int>(B - row0 < kBM ? B - row0 : kBM);
             const int nrows = clamp_rows(r0, r1, valid);
-            if (!pipe::wait(p, &rows_full[seg % kRowBufs], (seg / kRowBufs) & 1)) break;
+            if (!wait_count(p, &tickets[t], fs.P)) {
+                ok = false;
+                break;
+            }
             for (int tk = 0; tk < nrows && ok; ++tk) {
                 const uint16_t *xrow = X + (row0 + r0 + tk) * K;
                 for (int c0 = 0; c0 < C; c0 += W) {
@@ -376,7 +505,6 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                     if (++slot == kSlots) { slot = 0; slot_phase ^= 1; }
                 }
             }
-            ++seg;
         }
         if (!ok) {
             // let the bulk copies in flight land before shared memory is released
@@ -426,15 +554,19 @@ Plan make_plan(int64_t B, int n, int64_t C, int num_sms)
     const int kbt = static_cast<int>((K + kBK - 1) / kBK);
     const int64_t tile_bytes = static_cast<int64_t>(kBM) * K * 2;
     if (m_tiles < 2 || m_tiles > (int64_t{1} << 24)) return pl;
+    // two or more partial buffers: a CTA parks tile t before it finishes the
+    // tile before, so one buffer would have every CTA wait for the others
+    const int nb = kLeadChunks + 1 < kMaxPartBufs ? kLeadChunks + 1 : kMaxPartBufs;
+    if (kLeadChunks < 2 || nb < 2) return pl;
     for (int CH : {8, 4, 2, 1}) {
         const int P = num_sms / CH;
         if (CH > m_tiles || CH * tile_bytes > kChunkBytes || P < kBM / kMaxRows || kbt < P)
             continue;
         pl.fs = FSched{static_cast<int>(m_tiles), kbt, CH, P,
-                       static_cast<int>((m_tiles + CH - 1) / CH)};
+                       static_cast<int>((m_tiles + CH - 1) / CH), kLeadChunks, nb};
         pl.grid = CH * P;
         pl.ws_bytes = counts_bytes(static_cast<int>(m_tiles)) +
-                      2 * static_cast<size_t>(pl.grid) * kBM * (N + 1) * sizeof(float);
+                      static_cast<size_t>(pl.fs.nb) * pl.grid * kBM * (N + 1) * sizeof(float);
         pl.ok = true;
         break;
     }
@@ -460,7 +592,8 @@ cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const Plan &p
         configured |= 1ull << device;
     }
     const int m_tiles = pl.fs.m_tiles;
-    return launch_pdl(fused_pre_kernel<n>, dim3(pl.grid), dim3(kThreads), F::kSmemBytes, stream,
+    // cooperative: the CTAs wait on one another, so all of them must be resident
+    return launch_coop_pdl(fused_pre_kernel<n>, dim3(pl.grid), dim3(kThreads), F::kSmemBytes, stream,
                       tx, tw, B, static_cast<int>(n * C), static_cast<int>(C), pl.fs, a_pre,
                       a_post, a_res, bias, iters, X, Y, r, H_pre, H_post, H_res, F_pre, counts,
                       counts + m_tiles, partials, kWaitLimitNs);
