@@ -178,6 +178,9 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
             if (grow < B) mine[N] = ss;
         }
     }
+    // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before
+    // the CTA barrier, which needs whole warps
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 1) {
@@ -193,6 +196,7 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
         atomicAdd(grid_bar, 1u);
         if (!*p.abort && !wait_arrivals(grid_bar, bar_target, wait_limit_ns)) pipe::raise_timeout(p);
     }
+    __syncwarp();  // warp 0 whole again before the CTA barrier
     __syncthreads();
     if (*p.abort) return;
     // the X_next kernel may start launching; it waits for this grid to finish

@@ -516,6 +516,9 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
         }
     }
 
+    // lane 0 of the TMA, MMA and loader warps ran alone: reconverge every warp before
+    // the CTA barrier, which needs whole warps
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::pdl_trigger();  // at the end, as in the standalone GEMM

@@ -44,8 +44,8 @@ using pipe::SegIter;
 
 constexpr int kThreads = 320;  // 10 warps: TMA, MMA, 4 × square-sum, 4 × epilogue
 constexpr int kEpiThreads = 128;
-constexpr int kReduceItems = 4;   // outputs per thread per round of the fixed-order sum
-constexpr int kReduceBatch = 8;   // contributors loaded per batch: 32 loads in flight
+constexpr int kReduceItems = 16;  // outputs per thread per round of the fixed-order sum
+constexpr int kReduceBatch = 4;   // contributors loaded per batch: 64 loads in flight
 constexpr int kRingBudget = 200 * 1024;
 
 __device__ int g_device_status;
@@ -124,17 +124,24 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int64_t grow = row0 + row;
             const bool whole = sg.k0 == 0 && sg.k1 == sch.kbt;
             const int stride = N + 1;
+            // a partial is column-major, [N + 1][kBM]: stores and loads coalesce
             float *mine = partials + static_cast<int64_t>(cta + sg.m) * kBM * stride;
             float ss;
             if constexpr (kSplit) {
                 // chunks of 32 accumulator columns = 16 weight columns
-                float *dst = whole ? Y + grow * N : mine + row * stride;
                 const bool ok = pipe::take_accumulator_chunked<NPAD>(
                     p, seg, q, lane, ss, [&](int c, const float (&v)[32]) {
                         if (grow >= B) return;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (c * 16 + e < N) dst[c * 16 + e] = v[2 * e] + v[2 * e + 1];
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = c * 16 + e;
+                            if (j >= N) continue;
+                            const float y = v[2 * e] + v[2 * e + 1];
+                            if (whole)
+                                Y[grow * N + j] = y;
+                            else
+                                mine[j * kBM + row] = y;
+                        }
                     });
                 if (!ok) break;
                 ++seg;
@@ -142,7 +149,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     if (grow < B) r[grow] = sqrtf(ss / static_cast<float>(K));
                     continue;
                 }
-                if (grow < B) mine[row * stride + N] = ss;
+                if (grow < B) mine[N * kBM + row] = ss;
             } else {
                 float v[NPAD];
                 if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
@@ -158,12 +165,12 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     }
                     continue;
                 }
-                // partial: park [row][N+1] in this (cta, tile) slot, then take a ticket
+                // partial: park it in this (cta, tile) slot, then take a ticket
                 if (grow < B) {
 #pragma unroll
                     for (int j = 0; j < NPAD; ++j)
-                        if (j < N) mine[row * stride + j] = v[j];
-                    mine[row * stride + N] = ss;
+                        if (j < N) mine[j * kBM + row] = v[j];
+                    mine[N * kBM + row] = ss;
                 }
             }
             __threadfence();
@@ -179,8 +186,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 __threadfence();
                 // fixed-order sum over the contributors first..last: a batch of
                 // contributors x items is loaded before it is added, in order
-                const int64_t rows = (B - row0) < kBM ? (B - row0) : kBM;
-                const int items = static_cast<int>(rows) * stride;
+                const int rows = static_cast<int>((B - row0) < kBM ? (B - row0) : kBM);
+                const int items = kBM * stride;  // item i: column i / kBM, row i % kBM
                 const float *p0 = partials + static_cast<int64_t>(first + sg.m) * kBM * stride;
                 const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
                 const int nc = last - first + 1;
@@ -195,7 +202,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                             for (int u = 0; u < kReduceItems; ++u) {
                                 const int i = i0 + u * kEpiThreads;
-                                vb[c][u] = (c0 + c < nc && i < items)
+                                vb[c][u] = (c0 + c < nc && i < items && i % kBM < rows)
                                                ? __ldcg(p0 + (c0 + c) * slot_stride + i)
                                                : 0.f;  // acc + 0 is exact: acc is never -0
                             }
@@ -208,7 +215,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     for (int u = 0; u < kReduceItems; ++u) {
                         const int i = i0 + u * kEpiThreads;
                         if (i >= items) break;
-                        const int rr = i / stride, cc = i - rr * stride;
+                        const int rr = i % kBM, cc = i / kBM;
+                        if (rr >= rows) continue;
                         if (cc < N)
                             Y[(row0 + rr) * N + cc] = acc_s[u];
                         else
@@ -220,6 +228,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         }
     }
 
+    // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before
+    // the CTA barrier, which needs whole warps
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     // Let the next kernel launch only now: CTAs of a dependent kernel that sit

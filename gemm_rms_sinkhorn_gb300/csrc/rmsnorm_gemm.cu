@@ -257,6 +257,9 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
         }
     }
 
+    // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before
+    // the CTA barrier, which needs whole warps
+    __syncwarp();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::pdl_trigger();
