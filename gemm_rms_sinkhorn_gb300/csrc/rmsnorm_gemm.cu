@@ -20,7 +20,9 @@
 //   epilogue the accumulator leaves TMEM 32 columns at a time, is scaled by
 //            rstd, rounded to bf16 (RNE) and stored;
 //   pairs    with 256-column tiles and enough of them, clusters of two CTAs
-//            share each B box by multicast (see "CTA pairs" below).
+//            share each B box by multicast (see "CTA pairs" below);
+//   256 rows with 256-column tiles, long K and enough of them, a CTA takes
+//            256 × 256 tiles (see "256-row tiles" below).
 // The square sums of a row tile are computed once per run of its tiles in a
 // CTA, not once per column tile as on the page: the CUDA-core work is cheap,
 // but its shared-memory reads compete with the tensor cores' operand reads.
@@ -526,6 +528,322 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     }
 }
 
+// -------------------------------------------------------- 256-row tiles
+// With 256-column tiles and at least as many 256-row tiles as SMs, a CTA
+// takes 256 × 256 tiles: per K block one 256-row A box and one B box (64 KB),
+// two M=128 MMAs sharing the B operand into two 256-column accumulators (all
+// 512 TMEM columns).  That is 32 KB of stage per 4.2 MFLOP instead of 48, and
+// the ring's bytes against L2 latency are what bound the 128-row kernel.  The
+// accumulators are single-buffered: the epilogue frees the first as soon as it
+// has read it, so the next tile's first MMAs overlap the second half.
+constexpr int kBM2 = 2 * kBM;
+constexpr int kBoxA2 = kBM2 * kBK * 2;           // 32 KB
+constexpr int kBoxB2 = 256 * kBK * 2;            // 32 KB
+constexpr int kStage2 = kBoxA2 + kBoxB2;         // 64 KB
+constexpr int kStages2 = 3;
+constexpr int kSs2Bytes = 2 * kBM2 * 4;          // square sums, double-buffered
+constexpr int kBar2Bytes = 256;
+constexpr int kSmem2 = 1024 + kStages2 * kStage2 + kSs2Bytes + kBar2Bytes;
+static_assert(kSmem2 <= 227 * 1024, "shared memory");
+
+// Whole 256 × 256 tiles of a CTA, row tiles outermost.
+struct TIter {
+    int64_t t, end;
+    int n_tiles;
+    __device__ bool next(Segment &s) {
+        if (t >= end) return false;
+        s.m = static_cast<int>(t / n_tiles);
+        s.n = static_cast<int>(t - static_cast<int64_t>(s.m) * n_tiles);
+        s.k0 = 0;
+        s.k1 = 0;  // unused: every tile runs all K blocks
+        ++t;
+        return true;
+    }
+};
+
+struct M2Bars {
+    uint64_t *full, *empty;   // [kStages2]
+    uint64_t *acc_full;       // MMA -> epilogue, one phase per tile
+    uint64_t *acc_empty;      // [2] epilogue -> MMA, per accumulator
+    uint64_t *ss_full, *ss_empty;  // [2]
+    uint64_t *drain;
+    uint32_t *tmem_holder;
+};
+
+__device__ void m2_producer(const pipe::Pipe &p, const M2Bars &b, TIter it, int kbt,
+                            const CUtensorMap *tm_a, const CUtensorMap *tm_b)
+{
+    const uint64_t pol_a = ptx::policy_evict_normal();  // re-read by the next column tiles
+    const uint64_t pol_b = ptx::policy_evict_last();    // re-read by every row tile
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0, issued_parity = 0;
+    Segment sg;
+    bool ok = true;
+    while (ok && it.next(sg)) {
+        for (int kb = 0; kb < kbt; ++kb) {
+            if (!pipe::wait(p, &b.empty[stage], phase ^ 1)) {
+                ok = false;
+                break;
+            }
+            uint8_t *a = p.stages + stage * kStage2;
+            ptx::mbar_arrive_expect_tx(&b.full[stage], kStage2);
+            ptx::tma_load_2d(a, tm_a, kb * kBK, sg.m * kBM2, &b.full[stage], pol_a);
+            ptx::tma_load_2d(a + kBoxA2, tm_b, kb * kBK, sg.n * 256, &b.full[stage], pol_b);
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+    }
+    if (!ok) {
+        for (int s = 0; s < kStages2; ++s) {
+            if (!((issued_mask >> s) & 1u)) continue;
+            volatile int never = 0;
+            ptx::mbar_wait_bounded(&b.full[s], (issued_parity >> s) & 1u, &never, p.limit_ns);
+        }
+    }
+}
+
+__device__ void m2_mma_issuer(const pipe::Pipe &p, const M2Bars &b, TIter it, int kbt)
+{
+    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, 256);
+    int stage = 0;
+    uint32_t phase = 0;
+    int seg = 0;
+    Segment sg;
+    bool ok = true;
+    while (ok && it.next(sg)) {
+        const uint32_t epar = (seg & 1) ^ 1;  // each accumulator freed from the previous tile
+        for (int kb = 0; kb < kbt && ok; ++kb) {
+            if (!pipe::wait(p, &b.full[stage], phase)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t a_addr = ptx::smem_u32(p.stages + stage * kStage2);
+            const uint64_t b_desc = ptx::smem_desc_sw128(a_addr + kBoxA2);
+            for (int h = 0; h < 2; ++h) {
+                if (kb == 0) {
+                    if (!pipe::wait(p, &b.acc_empty[h], epar)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                }
+                // rows 128·h.. of the A box: 16 KB on, the same 128-byte swizzle
+                const uint64_t a_desc = ptx::smem_desc_sw128(a_addr + h * (kBoxA2 / 2));
+                const uint32_t d_tmem = p.tmem_base + static_cast<uint32_t>(h * 256);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
+                                  (kb > 0 || kk > 0) ? 1u : 0u);
+            }
+            if (!ok) break;
+            ptx::mma_commit(&b.empty[stage]);
+            if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        ptx::mma_commit(b.acc_full);
+        ++seg;
+    }
+    if (!ok || *p.abort) {
+        ptx::mma_commit(b.drain);
+        volatile int never = 0;
+        ptx::mbar_wait_bounded(b.drain, 0, &never, p.limit_ns);
+    }
+}
+
+// Σa² of one 128-byte stage row (64 bf16) into four partial sums.
+__device__ __forceinline__ void row_sq64(const uint8_t *arow, int row, float (&s)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        // chunk j of the row is at chunk j ^ (row % 8) (128-byte swizzle)
+        const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+        const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
+        const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
+        const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
+        s[0] = fmaf(a0, a0, s[0]); s[1] = fmaf(a1, a1, s[1]);
+        s[2] = fmaf(a2, a2, s[2]); s[3] = fmaf(a3, a3, s[3]);
+        s[0] = fmaf(a4, a4, s[0]); s[1] = fmaf(a5, a5, s[1]);
+        s[2] = fmaf(a6, a6, s[2]); s[3] = fmaf(a7, a7, s[3]);
+    }
+}
+
+// Thread t sums rows t and t + 128 of the tile; a tile of the previous tile's
+// row tile reuses its sums (see row_square_sums).
+__device__ void m2_square_sums(const pipe::Pipe &p, const M2Bars &b, TIter it, int kbt, int t,
+                               int lane)
+{
+    int stage = 0;
+    uint32_t phase = 0;
+    int seg = 0;
+    int prev_m = -1;
+    float prev0 = 0.f, prev1 = 0.f;
+    Segment sg;
+    bool ok = true;
+    while (ok && it.next(sg)) {
+        const bool reuse = sg.m == prev_m;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int kb = 0; kb < kbt; ++kb) {
+            if (!pipe::wait(p, &b.full[stage], phase)) {
+                ok = false;
+                break;
+            }
+            if (!reuse) {
+                const uint8_t *base = p.stages + stage * kStage2;
+                row_sq64(base + t * 128, t, s0);
+                row_sq64(base + (t + kBM) * 128, t + kBM, s1);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&b.empty[stage]);
+            if (++stage == kStages2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        const float ss0 = reuse ? prev0 : (s0[0] + s0[1]) + (s0[2] + s0[3]);
+        const float ss1 = reuse ? prev1 : (s1[0] + s1[1]) + (s1[2] + s1[3]);
+        const int buf = seg & 1;
+        if (!pipe::wait(p, &b.ss_empty[buf], ((seg >> 1) & 1) ^ 1)) break;
+        p.ss_buf[buf * kBM2 + t] = ss0;
+        p.ss_buf[buf * kBM2 + kBM + t] = ss1;
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&b.ss_full[buf]);
+        prev_m = sg.m;
+        prev0 = ss0;
+        prev1 = ss1;
+        ++seg;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+rmsnorm_gemm_m256_kernel(const __grid_constant__ CUtensorMap tm_a,
+                         const __grid_constant__ CUtensorMap tm_b, int64_t M, int64_t N, int K,
+                         float eps, int64_t tiles, int n_tiles, uint16_t *__restrict__ Cout,
+                         uint64_t wait_limit_ns)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    pipe::Pipe p{};
+    p.stages = smem;
+    p.ss_buf = reinterpret_cast<float *>(smem + kStages2 * kStage2);  // [2][256]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + kStages2 * kStage2 + kSs2Bytes);
+    M2Bars b;
+    b.full = bar;
+    b.empty = bar + kStages2;
+    b.acc_full = bar + 2 * kStages2;
+    b.acc_empty = b.acc_full + 1;
+    b.ss_full = b.acc_empty + 2;
+    b.ss_empty = b.ss_full + 2;
+    b.drain = b.ss_empty + 2;
+    b.tmem_holder = reinterpret_cast<uint32_t *>(b.drain + 1);
+    p.abort = reinterpret_cast<volatile int *>(b.tmem_holder + 1);
+    p.status = &g_rng_status;
+    p.limit_ns = wait_limit_ns;
+    p.stages_n = kStages2;
+    p.stage_bytes = kStage2;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int cta = blockIdx.x;
+    const int kbt = (K + kBK - 1) / kBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            ptx::mbar_init(&b.full[s], 1);
+            ptx::mbar_init(&b.empty[s], 1 + 4);  // MMA commit + one arrive per square-sum warp
+        }
+        ptx::mbar_init(b.acc_full, 1);
+        for (int a = 0; a < 2; ++a) {
+            ptx::mbar_init(&b.acc_empty[a], 4);
+            ptx::mbar_init(&b.ss_full[a], 4);
+            ptx::mbar_init(&b.ss_empty[a], 4);
+        }
+        ptx::mbar_init(b.drain, 1);
+        *p.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tm_a);
+        ptx::prefetch_tensormap(&tm_b);
+    }
+    if (warp == 1) ptx::tmem_alloc<512>(b.tmem_holder);
+    ptx::tc_fence_before();
+    __syncwarp();
+    __syncthreads();
+    ptx::tc_fence_after();
+    p.tmem_base = *b.tmem_holder;
+    ptx::pdl_wait();
+
+    const TIter segs{tiles * cta / gridDim.x, tiles * (cta + 1) / gridDim.x, n_tiles};
+    const float inv_k = 1.0f / static_cast<float>(K);
+
+    if (warp == 0) {
+        if (lane == 0) m2_producer(p, b, segs, kbt, &tm_a, &tm_b);
+    } else if (warp == 1) {
+        if (lane == 0) m2_mma_issuer(p, b, segs, kbt);
+    } else if (warp < 6) {
+        m2_square_sums(p, b, segs, kbt, (warp - 2) * 32 + lane, lane);
+    } else {
+        // ----------------------------------------------- epilogue (warps 6..9)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;
+        int seg = 0;
+        TIter it = segs;
+        Segment sg;
+        while (it.next(sg)) {
+            if (!pipe::wait(p, b.acc_full, seg & 1)) break;
+            ptx::tc_fence_after();
+            const int buf = seg & 1;
+            if (!pipe::wait(p, &b.ss_full[buf], (seg >> 1) & 1)) break;
+            const float ss0 = p.ss_buf[buf * kBM2 + row];
+            const float ss1 = p.ss_buf[buf * kBM2 + kBM + row];
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&b.ss_empty[buf]);
+            ++seg;
+            const int64_t col0 = static_cast<int64_t>(sg.n) * 256;
+            for (int h = 0; h < 2; ++h) {
+                const int64_t grow = static_cast<int64_t>(sg.m) * kBM2 + h * kBM + row;
+                const float rstd = rsqrtf((h ? ss1 : ss0) * inv_k + eps);
+                const uint32_t taddr = p.tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                       static_cast<uint32_t>(h * 256);
+#pragma unroll 1
+                for (int j = 0; j < 8; ++j) {
+                    float v[32], t16[16];
+                    ptx::tmem_ld_16(taddr + j * 32, t16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[e] = t16[e];
+                    ptx::tmem_ld_16(taddr + j * 32 + 16, t16);
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) v[16 + e] = t16[e];
+                    ptx::tmem_ld_wait();
+                    const int64_t c0 = col0 + j * 32;
+                    if (grow < M && c0 < N) {
+                        const int valid = N - c0 < 32 ? static_cast<int>(N - c0) : 32;
+                        store_cols32(v, rstd, Cout + grow * N + c0, valid);
+                    }
+                    __syncwarp();  // the next tcgen05.ld is warp-collective
+                }
+                // this accumulator may take the next tile's first MMAs
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&b.acc_empty[h]);
+            }
+        }
+    }
+
+    // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before
+    // the CTA barrier, which needs whole warps
+    __syncwarp();
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::pdl_trigger();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc<512>(p.tmem_base);
+    }
+}
+
 __global__ void zero_ints_kernel(int *p, int64_t count)
 {
     ptx::pdl_wait();
@@ -559,6 +877,39 @@ RSched rng_sched(int64_t M, int64_t K, int64_t N, int num_sms)
 }
 
 size_t tickets_bytes(int64_t tiles) { return (static_cast<size_t>(tiles) * 4 + 255) / 256 * 256; }
+
+// 256 × 256 tiles when every SM gets at least one and K has at least 64
+// blocks.  Their accumulators are single-buffered, so a tile's epilogue holds
+// up the next tile's first MMAs for a few µs; below 64 K blocks that costs more
+// than the smaller stages gain (measured: K = 4096 and 7168 13–23 % faster than
+// the pairs, K = 1024 and 2048 10–23 % slower).
+bool m256_ok(int64_t M, int64_t K, int64_t N, int num_sms)
+{
+    return tile_cols(N) == 256 && (K + kBK - 1) / kBK >= 64 &&
+           (M + kBM2 - 1) / kBM2 * ((N + 255) / 256) >= num_sms;
+}
+
+cudaError_t launch_m256(const uint16_t *A, const uint16_t *B_t, int64_t M, int64_t K, int64_t N,
+                        float eps, uint16_t *C, int num_sms, int device, cudaStream_t stream)
+{
+    CUtensorMap ta, tb;
+    if (!make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM2) ||
+        !make_tmap(&tb, B_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 256))
+        return cudaErrorInvalidValue;
+    static uint64_t configured = 0;  // one bit per device
+    static std::mutex mu;
+    if (device < 64 && !((configured >> device) & 1)) {
+        std::lock_guard<std::mutex> lock(mu);
+        cudaError_t e = cudaFuncSetAttribute(rmsnorm_gemm_m256_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem2);
+        if (e != cudaSuccess) return e;
+        configured |= 1ull << device;
+    }
+    const int64_t tiles = (M + kBM2 - 1) / kBM2 * ((N + 255) / 256);
+    return launch_pdl(rmsnorm_gemm_m256_kernel, dim3(num_sms), dim3(kThreads), kSmem2, stream,
+                      ta, tb, M, N, static_cast<int>(K), eps, tiles,
+                      static_cast<int>((N + 255) / 256), C, kWaitLimitNs);
+}
 
 // The CTA-pair schedule: 256-column tiles, pair tiles (two row tiles of one
 // column tile) split in whole pair tiles over num_sms / 2 pairs.  ok = false
@@ -637,7 +988,7 @@ cudaError_t launch_nt(const CUtensorMap &ta, const CUtensorMap &tb, int64_t M, i
 size_t rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N, int num_sms)
 {
     if (M <= 0) return 0;
-    if (pair_plan(M, K, N, num_sms).ok) return 0;
+    if (m256_ok(M, K, N, num_sms) || pair_plan(M, K, N, num_sms).ok) return 0;
     const RSched s = rng_sched(M, K, N, num_sms);
     if (s.aligned) return 0;
     const size_t slots = static_cast<size_t>(s.grid) + static_cast<size_t>(s.tiles);
@@ -652,6 +1003,7 @@ cudaError_t launch_rmsnorm_gemm(const uint16_t *A, const uint16_t *B_t, int64_t 
     int device = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    if (m256_ok(M, K, N, num_sms)) return launch_m256(A, B_t, M, K, N, eps, C, num_sms, device, stream);
     if (pp.ok) {
         CUtensorMap ta, tb;  // B in half boxes of 128 rows: one per CTA of a pair
         if (!make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM) ||
