@@ -285,9 +285,11 @@ int mhc_rmsnorm_gemm(const mhc_bf16 *A, const mhc_bf16 *B_t, int64_t M, int64_t 
 /*
  * Size of the built-in scratch array of mhc_gemm_rms_noalloc: 16 MiB, held in
  * device memory by every GPU that loads this library, until the process
- * exits.  A (B, n, C) fits when mhc_workspace_bytes(B, n, C) is at most this
- * (on a 152-SM GB300 the scratch does not depend on C: n=4 fits up to
- * B = 148,224 tokens, n=8 up to B = 32,256).
+ * exits.  A (B, n, C) fits when the GEMM's own split-K scratch (the part of
+ * mhc_workspace_bytes that mhc_gemm_rms checks) is at most this; on a 152-SM
+ * GB300 that scratch does not depend on C: n=4 fits up to B = 148,224 tokens,
+ * n=8 up to B = 32,256.  mhc_workspace_bytes itself may be larger: it also
+ * covers the other forward paths.
  */
 #define MHC_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 
