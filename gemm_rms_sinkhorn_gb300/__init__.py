@@ -41,6 +41,8 @@ _SIGS = {
     "mhc_workspace_bytes": ([_i64, _i32, _i64], _sz),
     "mhc_gemm_rms": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_coeffs": ([_vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _vp, _vp, _vp, _vp], _i32),
+    "mhc_gemm_rms_coeffs": ([_vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64, _vp, _vp,
+                             _vp, _vp, _vp, _vp, _sz, _vp], _i32),
     "mhc_pre_apply": ([_vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
     "mhc_post_res_apply": ([_vp, _vp, _vp, _vp, _i64, _i32, _i64, _vp, _vp], _i32),
     "mhc_forward": ([_vp, _vp, _vp, _f32, _f32, _f32, _vp, _i32, _i64, _i32, _i64,
@@ -169,6 +171,18 @@ def mhc_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
                            _ptr(bias, f, "bias"), iters, B, n, _ptr(H_pre, f, "H_pre"),
                            _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"), _stream(stream)),
            "mhc_coeffs")
+
+
+def mhc_gemm_rms_coeffs(X, phi_t, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C, Y, r,
+                        H_pre, H_post, H_res, ws, stream=None):
+    bf, f = torch.bfloat16, torch.float32
+    p, nb = _ws(ws)
+    _check(_lib.mhc_gemm_rms_coeffs(_ptr(X, bf, "X"), _ptr(phi_t, bf, "phi_t"), alpha_pre,
+                                    alpha_post, alpha_res, _ptr(bias, f, "bias"), iters, B, n, C,
+                                    _ptr(Y, f, "Y"), _ptr(r, f, "r"), _ptr(H_pre, f, "H_pre"),
+                                    _ptr(H_post, f, "H_post"), _ptr(H_res, f, "H_res"), p, nb,
+                                    _stream(stream)),
+           "mhc_gemm_rms_coeffs")
 
 
 def mhc_pre_apply(X, H_pre, B, n, C, F_pre, stream=None):

@@ -139,13 +139,14 @@ size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
     } while (0)
 
 // Batches up to this size take the one-launch steps 1-4a kernel.  Measured on
-// GB300 against the four-kernel chain: about 2x faster up to 512 tokens (the
+// GB300 against the kernel chain: about 2x faster up to 512 tokens (the
 // chain is bound by launch and reduction latency there), 10-45% faster at
-// 1024-2048, 4-7% at 3072, even at 4096 (n = 4 and 8, C = 256..7168).
+// 1024-2048 (n = 4 and 8, C = 256..7168); at 3072 the two are within 2%
+// (n = 4, C = 7168), and from 4096 the chain is faster.
 constexpr int64_t kDecodeMaxTokens = 3072;
 
 enum class Path {
-    Auto,           // decode_pre for small batches, else the four-kernel chain
+    Auto,           // decode_pre for small batches, else the kernel chain
     Chain,          // gemm_rms, coeffs, pre_apply
     Fused,          // fused_pre (test hook)
     Decode,         // decode_pre (test hook for any eligible batch)
@@ -162,6 +163,23 @@ size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
     if (f > w) w = f;
     if (d > w) w = d;
     return w;
+}
+
+// The coefficient arguments of the GEMM's finalize (steps 2 and 3).
+static CoefArgs coef_args(float a_pre, float a_post, float a_res, const float *bias, int iters,
+                          int n, float *H_pre, float *H_post, float *H_res)
+{
+    CoefArgs c;
+    c.bias = bias;
+    c.a_pre = a_pre;
+    c.a_post = a_post;
+    c.a_res = a_res;
+    c.iters = iters;
+    c.n = n;
+    c.H_pre = H_pre;
+    c.H_post = H_post;
+    c.H_res = H_res;
+    return c;
 }
 
 // The kernels of one forward for a path (arguments already valid and the path
@@ -185,10 +203,9 @@ static cudaError_t launch_forward(const uint16_t *X, const uint16_t *phi_t, cons
                               H_post, H_res, F_pre, workspace, num_sms, s, wait_limit_ns,
                               path == Path::DecodeStalled ? 1 : 0);
     } else {
-        e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, num_sms, s);
-        if (e == cudaSuccess)
-            e = launch_coeffs(Y, r, a_pre, a_post, a_res, bias, iters, B, n, H_pre, H_post,
-                              H_res, s);
+        // steps 1-3: the GEMM's finalize forms the coefficients of each finished token
+        e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, num_sms, s, kWaitLimitNs, -1,
+                            coef_args(a_pre, a_post, a_res, bias, iters, n, H_pre, H_post, H_res));
         if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
     }
     if (e == cudaSuccess) e = launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next, s);
@@ -336,6 +353,38 @@ int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post
     MHC_TRY(check_device(&info));
     return cuda_status(launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
                                      H_pre, H_post, H_res, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_gemm_rms_coeffs(const mhc_bf16 *X, const mhc_bf16 *phi_t, float alpha_pre,
+                        float alpha_post, float alpha_res, const float *bias, int iters,
+                        int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                        float *H_post, float *H_res, void *workspace, size_t workspace_bytes,
+                        mhc_stream_t stream)
+{
+    MHC_TRY(check_shape(B, n, C, true));
+    if (iters < 0) return MHC_ERR_INVALID;
+    if (B == 0) return MHC_OK;
+    const int N = num_coeffs(n);
+    const int64_t K = n * C;
+    const Buf ins[] = {{X, bf16_bytes(B * K)}, {phi_t, bf16_bytes(int64_t{N} * K)},
+                       {bias, f32_bytes(N)}};
+    Buf outs[] = {{Y, f32_bytes(B * N)},         {r, f32_bytes(B)},
+                  {H_pre, f32_bytes(B * n)},     {H_post, f32_bytes(B * n)},
+                  {H_res, f32_bytes(B * n * n)}, {workspace, workspace_bytes}};
+    MHC_TRY(check_ptrs(ins, 3));
+    MHC_TRY(check_ptrs(outs, 5));
+    MHC_TRY(check_overlap(outs, 5, ins, 3, nullptr, nullptr));
+    DeviceInfo info;
+    MHC_TRY(check_device(&info));
+    const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
+    if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
+    outs[5].bytes = need;
+    MHC_TRY(check_ptrs(outs + 5, 1));
+    MHC_TRY(check_overlap(outs, 6, ins, 3, nullptr, nullptr));
+    return cuda_status(launch_gemm_rms(
+        X, phi_t, B, n, C, Y, r, workspace, info.num_sms, reinterpret_cast<cudaStream_t>(stream),
+        kWaitLimitNs, -1,
+        coef_args(alpha_pre, alpha_post, alpha_res, bias, iters, n, H_pre, H_post, H_res)));
 }
 
 int mhc_pre_apply(const mhc_bf16 *X, const float *H_pre, int64_t B, int n, int64_t C,
@@ -528,10 +577,9 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
                               C, Y, r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
                               kWaitLimitNs, 0, true);
     } else {
-        e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s);
-        if (e == cudaSuccess)
-            e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
-                              H_post, H_res, s);
+        e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s,
+                                  coef_args(alpha_pre, alpha_post, alpha_res, bias, iters, n,
+                                            H_pre, H_post, H_res));
         if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
     }
     if (e == cudaSuccess)
@@ -636,10 +684,9 @@ int mhc_forward_e4m3(const uint8_t *X, const uint8_t *phi_t, const uint8_t *F_ou
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s);
-    if (e == cudaSuccess)
-        e = launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, H_pre,
-                          H_post, H_res, s);
+    cudaError_t e = launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s,
+                                         coef_args(alpha_pre, alpha_post, alpha_res, bias, iters,
+                                                   n, H_pre, H_post, H_res));
     if (e == cudaSuccess) e = launch_pre_apply_e4m3(X, H_pre, B, n, C, F_pre, s);
     if (e == cudaSuccess)
         e = launch_post_res_apply_e4m3(X, F_out, H_res, H_post, B, n, C, X_next, s);

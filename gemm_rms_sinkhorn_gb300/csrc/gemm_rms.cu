@@ -57,6 +57,38 @@ struct KCfg {
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
+// Steps 2 and 3 for the token of one finished row (CoefArgs): n is fixed by
+// the kernel's MMA width for all but a few (NPAD 16: n = 1, 2, 3; 48: n = 5,
+// 6), so only the n whose width matches are compiled in.
+template <int NPAD, bool kSplit, int nn>
+constexpr bool kWidthOf = ((kSplit ? 2 : 1) * (nn * nn + 2 * nn) + 15) / 16 * 16 == NPAD;
+
+template <int NPAD, bool kSplit, int nn>
+__device__ __forceinline__ void row_coeffs_n(const CoefArgs &cf, const float *y, float rb,
+                                             int64_t t)
+{
+    if constexpr (kWidthOf<NPAD, kSplit, nn>) {
+        if (cf.n == nn) {
+            float hp[nn], hq[nn], m[nn][nn];
+            token_coeffs<nn>(y, rb, cf.bias, cf.a_pre, cf.a_post, cf.a_res, cf.iters, hp, hq, m);
+            store_token_coeffs<nn>(t, hp, hq, m, cf.H_pre, cf.H_post, cf.H_res);
+        }
+    }
+}
+
+template <int NPAD, bool kSplit>
+__device__ __forceinline__ void row_coeffs(const CoefArgs &cf, const float *y, float rb, int64_t t)
+{
+    row_coeffs_n<NPAD, kSplit, 1>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 2>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 3>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 4>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 5>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 6>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 7>(cf, y, rb, t);
+    row_coeffs_n<NPAD, kSplit, 8>(cf, y, rb, t);
+}
+
 // kSplit: the weight operand holds every column twice, as the bf16 value
 // nearest the fp32 weight and the bf16 value nearest the remainder (rows 2k,
 // 2k+1 of φᵀ), and the epilogue adds each pair: Ỹ[k] = acc[2k] + acc[2k+1].
@@ -66,7 +98,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 int64_t B, int N, int K, Sched sch, float *__restrict__ Y, float *__restrict__ r,
                 int *__restrict__ tile_tickets, float *__restrict__ partials,
-                uint64_t wait_limit_ns, int64_t stall_stage)
+                uint64_t wait_limit_ns, int64_t stall_stage, CoefArgs cf)
 {
     using C = typename KCfg<NPAD>::C;
     extern __shared__ uint8_t smem_raw[];
@@ -146,7 +178,12 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (!ok) break;
                 ++seg;
                 if (whole) {
-                    if (grow < B) r[grow] = sqrtf(ss / static_cast<float>(K));
+                    if (grow < B) {
+                        const float rr = sqrtf(ss / static_cast<float>(K));
+                        r[grow] = rr;
+                        // this thread's own stores of the row, read back
+                        if (cf.H_pre) row_coeffs<NPAD, kSplit>(cf, Y + grow * N, rr, grow);
+                    }
                     continue;
                 }
                 if (grow < B) mine[N * kBM + row] = ss;
@@ -161,7 +198,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
 #pragma unroll
                         for (int j = 0; j < NPAD; ++j)
                             if (j < N) y[j] = v[j];
-                        r[grow] = sqrtf(ss / static_cast<float>(K));
+                        const float rr = sqrtf(ss / static_cast<float>(K));
+                        r[grow] = rr;
+                        if (cf.H_pre) row_coeffs<NPAD, kSplit>(cf, v, rr, grow);
                     }
                     continue;
                 }
@@ -223,6 +262,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                             r[row0 + rr] = sqrtf(acc_s[u] / static_cast<float>(K));
                     }
                 }
+                // thread et wrote all of row et (i % 128 == et): its coefficients
+                if (cf.H_pre && et < rows)
+                    row_coeffs<NPAD, kSplit>(cf, Y + (row0 + et) * N, r[row0 + et], row0 + et);
                 if (et == 0) tile_tickets[sg.m] = 0;
             }
         }
@@ -292,6 +334,7 @@ struct LaunchArgs {
     int device;
     uint64_t wait_limit_ns;
     int64_t stall_stage;
+    CoefArgs coef;
 };
 
 template <int NPAD, bool kSplit, bool kFp8 = false>
@@ -310,7 +353,7 @@ cudaError_t launch_cfg(const LaunchArgs &a)
     }
     return launch_pdl(gemm_rms_kernel<NPAD, kSplit, kFp8>, dim3(a.s.grid), dim3(kThreads),
                       Cf::kSmemBytes, a.stream, *a.tx, *a.tw, a.B, a.N, a.K, a.s, a.Y, a.r,
-                      a.tickets, a.partials, a.wait_limit_ns, a.stall_stage);
+                      a.tickets, a.partials, a.wait_limit_ns, a.stall_stage, a.coef);
 }
 
 cudaError_t dispatch(int npad, bool split, bool fp8, const LaunchArgs &a)
@@ -428,7 +471,8 @@ size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
 static cudaError_t launch_gemm_rms_impl(const void *X, const void *phi_t, int64_t B, int n,
                                         int64_t C, float *Y, float *r, void *workspace,
                                         int num_sms, cudaStream_t stream, uint64_t wait_limit_ns,
-                                        int64_t stall_stage, bool split, bool fp8)
+                                        int64_t stall_stage, bool split, bool fp8,
+                                        const CoefArgs &coef)
 {
     const int N = num_coeffs(n);
     const int64_t K = n * C;
@@ -451,32 +495,33 @@ static cudaError_t launch_gemm_rms_impl(const void *X, const void *phi_t, int64_
     int device = 0;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     const LaunchArgs a{&tx, &tw, B, N, static_cast<int>(K), s, Y, r, tickets, partials, stream,
-                       device, wait_limit_ns, stall_stage};
+                       device, wait_limit_ns, stall_stage, coef};
     return dispatch(npad, split, fp8, a);
 }
 
 cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
                             int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                            cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage)
+                            cudaStream_t stream, uint64_t wait_limit_ns, int64_t stall_stage,
+                            const CoefArgs &coef)
 {
     return launch_gemm_rms_impl(X, phi_t, B, n, C, Y, r, workspace, num_sms, stream,
-                                wait_limit_ns, stall_stage, false, false);
+                                wait_limit_ns, stall_stage, false, false, coef);
 }
 
 cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, int64_t B, int n,
                                   int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                                  cudaStream_t stream)
+                                  cudaStream_t stream, const CoefArgs &coef)
 {
     return launch_gemm_rms_impl(X, phi_split, B, n, C, Y, r, workspace, num_sms, stream,
-                                kWaitLimitNs, -1, true, false);
+                                kWaitLimitNs, -1, true, false, coef);
 }
 
 cudaError_t launch_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n,
                                  int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                                 cudaStream_t stream)
+                                 cudaStream_t stream, const CoefArgs &coef)
 {
     return launch_gemm_rms_impl(X, phi_t, B, n, C, Y, r, workspace, num_sms, stream,
-                                kWaitLimitNs, -1, false, true);
+                                kWaitLimitNs, -1, false, true, coef);
 }
 
 cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,

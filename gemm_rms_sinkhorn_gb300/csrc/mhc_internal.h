@@ -69,24 +69,33 @@ cudaError_t current_device_info(DeviceInfo *info);
 // Every wait inside the GEMM kernel gives up after this much GPU time.
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 size_t gemm_rms_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
+// Steps 2 and 3 folded into the GEMM's finalize: with H_pre non-null, the CTA
+// that writes a token's Y and r also forms its H_pre, H_post and H_res
+// (token_coeffs, the coefficient kernel's computation, so the same bits).
+struct CoefArgs {
+    const float *bias = nullptr;
+    float a_pre = 0.f, a_post = 0.f, a_res = 0.f;
+    int iters = 0, n = 0;
+    float *H_pre = nullptr, *H_post = nullptr, *H_res = nullptr;
+};
 // stall_stage >= 0 is a test hook: CTA 0 leaves that pipeline stage unfilled.
 cudaError_t launch_gemm_rms(const uint16_t *X, const uint16_t *phi_t, int64_t B, int n,
                             int64_t C, float *Y, float *r, void *workspace, int num_sms,
                             cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
-                            int64_t stall_stage = -1);
+                            int64_t stall_stage = -1, const CoefArgs &coef = CoefArgs{});
 cudaError_t read_and_clear_device_status(int *status);
 // The fp32-weight form: phi_split [2N][K] bf16 (hi and remainder of each
 // fp32 weight column, interleaved) from launch_split_phi; the same Y and r.
 cudaError_t launch_gemm_rms_split(const uint16_t *X, const uint16_t *phi_split, int64_t B, int n,
                                   int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                                  cudaStream_t stream);
+                                  cudaStream_t stream, const CoefArgs &coef = CoefArgs{});
 cudaError_t launch_split_phi(const float *phi_t, int n, int64_t C, uint16_t *phi_split,
                              cudaStream_t stream);
 // The fp8 form: X [B][K] and phi_t [N][K] as e4m3 codes (kind::f8f6f4 MMAs,
 // 128 K values per stage); the same Y, r and workspace.
 cudaError_t launch_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n,
                                  int64_t C, float *Y, float *r, void *workspace, int num_sms,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const CoefArgs &coef = CoefArgs{});
 
 // Tensor map of a 2-D bf16 tensor [rows][cols] (cols contiguous): boxes of
 // box_rows × 64 elements, 128-byte swizzle, zero fill out of bounds.
@@ -120,7 +129,7 @@ cudaError_t read_and_clear_decode_status(int *status);
 // Workspace of every forward path (and of mhc_gemm_rms), whichever is largest.
 size_t forward_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
 // mhc_forward's own choice of path: the one-launch steps 1-4a kernel for small
-// batches, else the four-kernel chain; then the X_next kernel.
+// batches, else the kernel chain; then the X_next kernel.
 cudaError_t run_forward_device(const uint16_t *X, const uint16_t *phi_t, const uint16_t *F_out,
                                float a_pre, float a_post, float a_res, const float *bias,
                                int iters, int64_t B, int n, int64_t C, float *Y, float *r,

@@ -12,9 +12,11 @@
  *                       H_post = 2σ(H̃_post), H_res = Sinkhorn(H̃_res) (§2.3, §2.4, §3.2, §3.3)
  *   mhc_pre_apply       F_pre = Σ_i H_pre[i]·X[i]                 (§2.5)
  *   mhc_post_res_apply  X_next[i] = Σ_j H_res[i][j]·X[j] + H_post[i]·F_out (§2.5, §3.4)
- *   mhc_forward         steps 1-4b on one stream (the four calls above, or for
- *                       B <= 3072 steps 1-4a in one launch, then step 4b)
+ *   mhc_forward         steps 1-4b on one stream (mhc_gemm_rms_coeffs, mhc_pre_apply,
+ *                       mhc_post_res_apply, or for B <= 3072 steps 1-4a in one
+ *                       launch, then step 4b)
  *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
+ *   mhc_gemm_rms_coeffs steps 1-3 in one launch (mhc_gemm_rms then mhc_coeffs)
  *   mhc_rmsnorm_gemm    C = rmsnorm(A) @ B for any N (Lazy Pre-Norm, second page §2)
  *   mhc_*_f32w / _split / _f32   the fp32-weight, fp32-F_out precision variant (§5)
  *   mhc_*_e4m3          the fp8 e4m3 precision variant (§4)
@@ -110,11 +112,25 @@ int mhc_gemm_rms(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, int n, int
  *   H_res     = Sinkhorn–Knopp: start from exp(H̃_res) as an n×n matrix, then
  *               `iters` times divide each row by its sum, then each column
  *               by its sum.  iters = 0 returns exp(H̃_res) unnormalised.
- * The n×n iteration runs in registers: n lanes of a warp per token, one row per lane.
+ * One thread per token holds the n×n block in registers through the iteration.
  */
 int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post,
                float alpha_res, const float *bias, int iters, int64_t B, int n,
                float *H_pre, float *H_post, float *H_res, mhc_stream_t stream);
+
+/*
+ * Steps 1–3 in one launch: mhc_gemm_rms, then mhc_coeffs folded into the
+ * GEMM's finalize.  The CTA that writes a token's Y and r forms its H_pre,
+ * H_post and H_res with the same arithmetic as mhc_coeffs, so the results are
+ * those of the two calls in sequence, bit for bit.  Arguments, layouts and the
+ * workspace are those of mhc_gemm_rms and mhc_coeffs; mhc_forward's chain
+ * runs steps 1–3 this way.
+ */
+int mhc_gemm_rms_coeffs(const mhc_bf16 *X, const mhc_bf16 *phi_t, float alpha_pre,
+                        float alpha_post, float alpha_res, const float *bias, int iters,
+                        int64_t B, int n, int64_t C, float *Y, float *r, float *H_pre,
+                        float *H_post, float *H_res, void *workspace, size_t workspace_bytes,
+                        mhc_stream_t stream);
 
 /*
  * Step 4a — pre-mixing, n streams to one (§2.5 (1)):
@@ -143,7 +159,8 @@ int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_
  * Path: for B <= 3072 steps 1-4a run as one cooperative launch (the split-K
  * GEMM over every SM, a bounded grid barrier, then each CTA's fixed-order
  * reduction, coefficients and F_pre), which measured faster than the
- * four-kernel chain at those sizes; above, the chain.  Either path is
+ * kernel chain at those sizes; above, the chain (mhc_gemm_rms_coeffs,
+ * mhc_pre_apply, mhc_post_res_apply).  Either path is
  * deterministic; they differ in the split-K order, so Y (and what follows
  * from it) differs between them in the last bits, within the tolerances.
  */
@@ -211,7 +228,7 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
  *   mhc_post_res_apply_f32  mhc_post_res_apply with F_out [B][C] fp32;
  *   mhc_forward_f32w    the forward with both (X, F_pre, X_next bf16): like
  *                       mhc_forward, steps 1-4a in one launch for B <= 3072,
- *                       else the four-kernel chain; workspace of
+ *                       else the kernel chain; workspace of
  *                       mhc_workspace_bytes.
  * Rules, layouts and status codes otherwise as the bf16 calls.
  */
@@ -240,7 +257,7 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
  * outputs to nearest even, saturating to ±448.
  * Rules of the bf16 calls, plus C % 16 == 0 (MHC_ERR_UNSUPPORTED otherwise);
  * the workspace is mhc_workspace_bytes(B, n, C).  mhc_forward_e4m3 always runs
- * the four-kernel chain.
+ * the kernel chain (GEMM with the coefficients, then the two applies).
  */
 int mhc_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n, int64_t C,
                       float *Y, float *r, void *workspace, size_t workspace_bytes,

@@ -50,7 +50,7 @@ int mhc_testing_forward_fused(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mh
                               size_t workspace_bytes, mhc_stream_t stream);
 
 /*
- * mhc_forward forced onto the four-kernel chain (mhc_gemm_rms, mhc_coeffs,
+ * mhc_forward forced onto the kernel chain (mhc_gemm_rms_coeffs,
  * mhc_pre_apply, mhc_post_res_apply), which mhc_forward itself takes only
  * above its small-batch threshold.  Same arguments, rules and outputs as
  * mhc_forward.

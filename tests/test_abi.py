@@ -62,6 +62,12 @@ def coeffs(Y=A, r=B_, bias=C_, iters=20, Bt=4, n=4, hp=D, hq=E, hr=F):
     return L.mhc_coeffs(Y, r, 0.01, 0.01, 0.01, bias, iters, Bt, n, hp, hq, hr, None)
 
 
+def gemm_coeffs(X=A, phi=B_, bias=C_, iters=20, Bt=4, n=4, C=256, Y=D, r=E, hp=F, hq=G, hr=H,
+                ws=W, wsb=1 << 30):
+    return L.mhc_gemm_rms_coeffs(X, phi, 0.01, 0.01, 0.01, bias, iters, Bt, n, C, Y, r, hp, hq,
+                                 hr, ws, wsb, None)
+
+
 def pre(X=A, Hp=B_, Bt=4, n=4, C=256, Fp=C_):
     return L.mhc_pre_apply(X, Hp, Bt, n, C, Fp, None)
 
@@ -82,12 +88,13 @@ NO_DEVICE = mhc.MHC_ERR_CUDA  # valid host arguments reach the device check
 def test_empty_batch_is_a_noop():
     assert gemm(Bt=0, X=None, phi=None, Y=None, r=None, ws=None, wsb=0) == mhc.MHC_OK
     assert coeffs(Bt=0) == mhc.MHC_OK
+    assert gemm_coeffs(Bt=0) == mhc.MHC_OK
     assert pre(Bt=0) == mhc.MHC_OK
     assert post(Bt=0) == mhc.MHC_OK
     assert fwd(Bt=0) == mhc.MHC_OK
 
 
-@pytest.mark.parametrize("call", [gemm, pre, post, fwd])
+@pytest.mark.parametrize("call", [gemm, gemm_coeffs, pre, post, fwd])
 def test_shape_rules(call):
     assert call(n=0) == mhc.MHC_ERR_UNSUPPORTED
     assert call(n=9) == mhc.MHC_ERR_UNSUPPORTED
@@ -99,6 +106,12 @@ def test_shape_rules(call):
 def test_coeffs_rules():
     assert coeffs(n=9) == mhc.MHC_ERR_UNSUPPORTED
     assert coeffs(iters=-1) == mhc.MHC_ERR_INVALID
+    assert gemm_coeffs(iters=-1) == mhc.MHC_ERR_INVALID
+    assert gemm_coeffs(bias=None) == mhc.MHC_ERR_INVALID
+    assert gemm_coeffs(hr=H + 4) == mhc.MHC_ERR_ALIGN
+    assert gemm_coeffs(hq=A + 64) == mhc.MHC_ERR_INVALID  # an output over X
+    assert gemm_coeffs(hp=G) == mhc.MHC_ERR_INVALID       # two outputs over each other
+    assert gemm_coeffs() == NO_DEVICE
     assert fwd(iters=-1) == mhc.MHC_ERR_INVALID
     assert coeffs(Y=None) == mhc.MHC_ERR_INVALID
 

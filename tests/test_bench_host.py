@@ -25,6 +25,16 @@ def test_algorithmic_bytes_prefill():
     assert sum(a.values()) == 4_235_657_312
 
 
+def test_kernel_bytes_prefill():
+    """Steps 1-3 in one kernel: the GEMM's bytes and the coefficients' bytes, less
+    the read-back of Y and r that no longer happens."""
+    k = bench.kernel_bytes(16384, 4, 7168)
+    assert set(k) == set(bench.KERNELS)
+    assert k["gemm_rms"] == 942_538_752 + 3_211_360 - (4 * 16384 * 24 + 4 * 16384)
+    assert k["pre_apply"] == 1_174_667_264
+    assert k["post_res_apply"] == 2_115_239_936
+
+
 def test_tokens_per_second_is_whole_job():
     assert bench.tokens_per_second(16384, 4, 10, 1000.0) == 16384 * 4 * 10
     assert bench.max_over_ranks(3.5) == 3.5

@@ -284,6 +284,30 @@ def test_forward_prefill_full_size_sampled():
     assert torch.equal(Y0, out2["Y"]) and torch.equal(X0, out2["X_next"])
 
 
+# steps 1-3 in one launch (the GEMM's finalize forms the coefficients): tiles
+# split over many CTAs, whole tiles owned by one CTA (K = 64: one unit each),
+# every n, ragged last tiles
+GEMM_COEFF_SHAPES = [(64, 4, 256), (1000, 4, 7168), (300, 8, 512), (5, 3, 24), (777, 1, 1000),
+                     (2048, 6, 2048), (40000, 1, 64), (20000, 2, 32), (700, 5, 168), (900, 7, 96)]
+
+
+@pytest.mark.parametrize("B,n,C", GEMM_COEFF_SHAPES)
+def test_gemm_rms_coeffs_equals_the_two_calls(B, n, C):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=21)
+    X, phi, bias = dev_bf16(inp["X"]), dev_bf16(inp["phi_t"]), dev_f32(inp["bias"])
+    a, b = mhc.alloc_outputs(B, n, C), mhc.alloc_outputs(B, n, C)
+    mhc.mhc_gemm_rms(X, phi, B, n, C, a["Y"], a["r"], a["ws"])
+    mhc.mhc_coeffs(a["Y"], a["r"], wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias, wl.iters, B,
+                   n, a["H_pre"], a["H_post"], a["H_res"])
+    mhc.mhc_gemm_rms_coeffs(X, phi, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias, wl.iters, B,
+                            n, C, b["Y"], b["r"], b["H_pre"], b["H_post"], b["H_res"], b["ws"])
+    torch.cuda.synchronize()
+    for k in ("Y", "r", "H_pre", "H_post", "H_res"):
+        assert torch.equal(a[k], b[k]), k
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+
+
 # shapes for the one-kernel steps 1-4a path (test hook): a ragged last tile, a
 # ragged last chunk of tiles, n=8, a single chunk, and the 7B-width workload
 FUSED_SHAPES = [(1000, 4, 7168), (1100, 4, 4096), (600, 8, 2048), (256, 4, 2048), (4096, 4, 4096)]
