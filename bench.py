@@ -437,7 +437,7 @@ def main() -> int:
                     help="seconds of identical load kept up for the clock samples")
     ap.add_argument("--path", default="auto", choices=["auto", "chain", "decode", "fused"],
                     help="forward path of each step: auto (mhc_forward's own choice) or one "
-                         "forced through its test hook: chain (four kernels), decode (the "
+                         "forced through its test hook: chain (three kernels), decode (the "
                          "small-batch one-launch steps 1-4a), fused (the large-batch one-kernel "
                          "steps 1-4a)")
     ap.add_argument("--precision", default="bf16", choices=["bf16", "f32w", "e4m3"],

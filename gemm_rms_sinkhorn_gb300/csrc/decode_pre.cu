@@ -3,7 +3,7 @@
 // Sinkhorn–Knopp projection (§2.3, §2.4), and F_pre (§2.5 (1)), page "mHC 算法
 // 分析 & cutile 高效实现".  With a few tokens the forward is a chain of
 // latencies, not of bytes (§3.2 counts the launches, §5.1 the idle SMs), so
-// this kernel replaces four launches by one and spreads the GEMM over every SM.
+// this kernel replaces the chain's launches by one and spreads the GEMM over every SM.
 //
 //   phase 1  the stream-K X·φ + Σx² pipeline of gemm_pipeline.cuh over all SMs;
 //            every CTA parks its partial sums (one slot per CTA and token tile);
