@@ -263,6 +263,23 @@ __device__ void pair_mma_issuer(const pipe::Pipe &p, PIter it)
     }
 }
 
+// Σa² of one 128-byte stage row (64 bf16) into four partial sums.
+__device__ __forceinline__ void row_sq64(const uint8_t *arow, int row, float (&s)[4])
+{
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        // chunk j of the row is at chunk j ^ (row % 8) (128-byte swizzle)
+        const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+        const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
+        const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
+        const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
+        s[0] = fmaf(a0, a0, s[0]); s[1] = fmaf(a1, a1, s[1]);
+        s[2] = fmaf(a2, a2, s[2]); s[3] = fmaf(a3, a3, s[3]);
+        s[0] = fmaf(a4, a4, s[0]); s[1] = fmaf(a5, a5, s[1]);
+        s[2] = fmaf(a6, a6, s[2]); s[3] = fmaf(a7, a7, s[3]);
+    }
+}
+
 // As pipe::square_sum (bf16), but a whole tile whose row tile is that of the
 // previous whole tile hands over the previous sum without reading its stages:
 // the A rows, hence Σa², are the same.  Shared-memory reads are what bound
@@ -282,40 +299,26 @@ __device__ void row_square_sums(const pipe::Pipe &p, It it, int kbt, int row, in
     while (ok && it.next(sg)) {
         const bool whole = sg.k0 == 0 && sg.k1 == kbt;
         const bool reuse = whole && sg.m == prev_m;
-        float ss0 = 0.f, ss1 = 0.f, ss2 = 0.f, ss3 = 0.f;
+        float ss[4] = {0.f, 0.f, 0.f, 0.f};
         for (int kb = sg.k0; kb < sg.k1; ++kb) {
             if (!pipe::wait(p, &p.full[stage], phase)) {
                 ok = false;
                 break;
             }
-            if (!reuse) {
-                const uint8_t *arow = p.stages + stage * p.stage_bytes + row * 128;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // chunk j of the row is at chunk j ^ (row % 8) (128-byte swizzle)
-                    const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
-                    const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
-                    const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
-                    const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
-                    ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
-                    ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
-                    ss0 = fmaf(a4, a4, ss0); ss1 = fmaf(a5, a5, ss1);
-                    ss2 = fmaf(a6, a6, ss2); ss3 = fmaf(a7, a7, ss3);
-                }
-            }
+            if (!reuse) row_sq64(p.stages + stage * p.stage_bytes + row * 128, row, ss);
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&p.empty[stage]);
             if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
-        const float ss = reuse ? prev_ss : (ss0 + ss1) + (ss2 + ss3);
+        const float sum = reuse ? prev_ss : (ss[0] + ss[1]) + (ss[2] + ss[3]);
         const int buf = seg & 1;
         if (!pipe::wait(p, &p.ss_empty[buf], ((seg >> 1) & 1) ^ 1)) break;
-        p.ss_buf[buf * kBM + row] = ss;
+        p.ss_buf[buf * kBM + row] = sum;
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&p.ss_full[buf]);
         prev_m = whole ? sg.m : -1;
-        prev_ss = ss;
+        prev_ss = sum;
         ++seg;
     }
 }
@@ -653,22 +656,6 @@ __device__ void m2_mma_issuer(const pipe::Pipe &p, const M2Bars &b, TIter it, in
     }
 }
 
-// Σa² of one 128-byte stage row (64 bf16) into four partial sums.
-__device__ __forceinline__ void row_sq64(const uint8_t *arow, int row, float (&s)[4])
-{
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        // chunk j of the row is at chunk j ^ (row % 8) (128-byte swizzle)
-        const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
-        const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
-        const float a3 = bf16_hi(v.y), a4 = bf16_lo(v.z), a5 = bf16_hi(v.z);
-        const float a6 = bf16_lo(v.w), a7 = bf16_hi(v.w);
-        s[0] = fmaf(a0, a0, s[0]); s[1] = fmaf(a1, a1, s[1]);
-        s[2] = fmaf(a2, a2, s[2]); s[3] = fmaf(a3, a3, s[3]);
-        s[0] = fmaf(a4, a4, s[0]); s[1] = fmaf(a5, a5, s[1]);
-        s[2] = fmaf(a6, a6, s[2]); s[3] = fmaf(a7, a7, s[3]);
-    }
-}
 
 // Thread t sums rows t and t + 128 of the tile; a tile of the previous tile's
 // row tile reuses its sums (see row_square_sums).
