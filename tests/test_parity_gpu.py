@@ -291,9 +291,11 @@ GEMM_COEFF_SHAPES = [(64, 4, 256), (1000, 4, 7168), (300, 8, 512), (5, 3, 24), (
                      (2048, 6, 2048), (40000, 1, 64), (20000, 2, 32), (700, 5, 168), (900, 7, 96)]
 
 
-@pytest.mark.parametrize("B,n,C", GEMM_COEFF_SHAPES)
-def test_gemm_rms_coeffs_equals_the_two_calls(B, n, C):
-    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3)
+@pytest.mark.parametrize("B,n,C,iters", [s + (20,) for s in GEMM_COEFF_SHAPES] +
+                         [(1000, 4, 7168, 0), (1000, 4, 7168, 1), (40000, 1, 64, 0),
+                          (300, 8, 512, 1)])
+def test_gemm_rms_coeffs_equals_the_two_calls(B, n, C, iters):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C, bias_std=0.3, iters=iters)
     inp = make_inputs(wl, seed=21)
     X, phi, bias = dev_bf16(inp["X"]), dev_bf16(inp["phi_t"]), dev_f32(inp["bias"])
     a, b = mhc.alloc_outputs(B, n, C), mhc.alloc_outputs(B, n, C)

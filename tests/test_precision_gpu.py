@@ -125,3 +125,11 @@ def test_forward_f32w_7b_sampled():
 
 def test_forward_f32w_wider_n8():
     forward_f32w(WORKLOADS["wider"].with_(B=300), seed=76)
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 6, 7, 8])
+def test_forward_f32w_chain_every_n(n):
+    """Above 3072 tokens the forward takes the kernel chain, whose split-weight GEMM forms
+    the coefficients in its finalize: one GEMM width per n (2N padded to 16)."""
+    wl = WORKLOADS["tiny"].with_(B=3200, n=n, C=64, bias_std=0.3)
+    forward_f32w(wl, seed=77 + n, rows=sample_rows(wl.B, 64))
