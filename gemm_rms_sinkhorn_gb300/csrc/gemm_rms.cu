@@ -297,12 +297,6 @@ __global__ void zero_tickets_kernel(int *tickets, int count)
 
 // ------------------------------------------------------------------ host
 
-int npad_of(int n)
-{
-    const int N = num_coeffs(n);
-    return (N + 15) / 16 * 16;
-}
-
 // Grid: one CTA per SM, but no more than 32 contributors per token tile (the
 // last arriver's fixed-order sum grows with the fan-in) and at least one
 // stage of K per CTA.
