@@ -72,7 +72,8 @@ int check_shape(int64_t B, int n, int64_t C, bool needs_c)
         // K = n*C is addressed with 32-bit TMA coordinates and int kernel arguments
         if (static_cast<int64_t>(n) * C > (int64_t{1} << 30)) return MHC_ERR_UNSUPPORTED;
     }
-    if (B > (int64_t{1} << 40)) return MHC_ERR_UNSUPPORTED;
+    // token rows are TMA coordinates, 32-bit signed
+    if (B >= (int64_t{1} << 31)) return MHC_ERR_UNSUPPORTED;
     return MHC_OK;
 }
 

@@ -44,7 +44,8 @@
  *
  * Argument rules (checked on the host; a failing call launches nothing):
  *   - B >= 0; B == 0 is a no-op that returns MHC_OK;
- *   - 1 <= n <= 8; C >= 8 and C % 8 == 0;  otherwise MHC_ERR_UNSUPPORTED;
+ *   - B < 2^31; 1 <= n <= 8; C >= 8, C % 8 == 0 and n*C <= 2^30;
+ *     otherwise MHC_ERR_UNSUPPORTED;
  *   - pointers non-NULL (MHC_ERR_INVALID) and 16-byte aligned (MHC_ERR_ALIGN);
  *   - an output may not overlap any input or another output
  *     (MHC_ERR_INVALID), except that X_next may be exactly X;
@@ -287,8 +288,8 @@ int mhc_forward_e4m3(const uint8_t *X, const uint8_t *phi_t, const uint8_t *F_ou
  *   A    [M][K] bf16
  *   B_t  [N][K] bf16   Bᵀ, K contiguous (a linear layer's weight [out][in])
  *   C    [M][N] bf16   fp32 accumulation and scaling, rounded to nearest even
- * Rules: M >= 0 (M == 0 is a no-op); 8 <= K <= 2^30 and 8 <= N <= 2^24, both
- * multiples of 8 (MHC_ERR_UNSUPPORTED); eps finite and >= 0 (MHC_ERR_INVALID);
+ * Rules: M >= 0 (M == 0 is a no-op); M < 2^31, 8 <= K <= 2^30 and
+ * 8 <= N <= 2^24, K and N multiples of 8 (MHC_ERR_UNSUPPORTED); eps finite and >= 0 (MHC_ERR_INVALID);
  * pointers non-NULL and 16-byte aligned; C may not overlap A or B_t.
  * workspace: mhc_rmsnorm_gemm_workspace_bytes(M, K, N) bytes of device memory
  * (0 when every CTA gets whole output tiles; then workspace may be NULL).

@@ -101,6 +101,7 @@ def test_shape_rules(call):
     assert call(C=12) == mhc.MHC_ERR_UNSUPPORTED
     assert call(C=0) == mhc.MHC_ERR_UNSUPPORTED
     assert call(Bt=-1) == mhc.MHC_ERR_INVALID
+    assert call(Bt=1 << 31) == mhc.MHC_ERR_UNSUPPORTED  # token rows are 32-bit TMA coordinates
 
 
 def test_coeffs_rules():
@@ -213,6 +214,8 @@ def test_rmsnorm_gemm_validates_on_the_host():
     assert f(A, B_, 16, 64, 64, -1.0, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
     assert f(A, B_, 16, 64, 64, float("nan"), C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
     assert f(A, B_, -1, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
+    assert f(A, B_, 1 << 31, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_UNSUPPORTED
+    assert f(A, B_, 16, 1 << 31, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_UNSUPPORTED
     assert f(None, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
     assert f(A + 8, B_, 16, 64, 64, 1e-5, C_, W, 1 << 30, None) == mhc.MHC_ERR_ALIGN
     assert f(A, B_, 16, 64, 64, 1e-5, A + 64, W, 1 << 30, None) == mhc.MHC_ERR_INVALID
