@@ -278,20 +278,31 @@ __device__ void square_sum(const Pipe &p, It it, int row, int lane)
                 break;
             }
             const uint8_t *arow = p.stages + stage * p.stage_bytes + row * 128;
+            // 16-byte chunk j of the row lives at chunk (j ^ row%8) (128-byte
+            // swizzle); a row sum needs every chunk once, in any order.
+            uint4 row_v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                row_v[j] = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+            const auto release = [&] {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&p.empty[stage]);  // release: orders the loads
+                if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
+            };
+            // e4m3 rows cost about three times the arithmetic of bf16 rows: their
+            // stage goes back before it, so the ring refills meanwhile (measured
+            // at B=16384, n=4, C=7168: 86.8 -> 85.6 us; the same order made the
+            // bf16 GEMM 1 us slower, so bf16 keeps arithmetic-then-release).
+            if constexpr (kFp8) release();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                // 16-byte chunk j of the row lives at chunk (j ^ row%8) (128-byte
-                // swizzle); a row sum needs every chunk once, in any order.
-                const uint4 v = *reinterpret_cast<const uint4 *>(arow + ((j ^ (row & 7)) << 4));
+                const uint4 v = row_v[j];
                 if constexpr (kFp8) {
                     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        float a0, a1, a2, a3;
-                        e4m3x2_to_f32(w[h], a0, a1);
-                        e4m3x2_to_f32(w[h] >> 16, a2, a3);
-                        ss0 = fmaf(a0, a0, ss0); ss1 = fmaf(a1, a1, ss1);
-                        ss2 = fmaf(a2, a2, ss2); ss3 = fmaf(a3, a3, ss3);
+                        e4m3x2_square_add(w[h], ss0, ss1);
+                        e4m3x2_square_add(w[h] >> 16, ss2, ss3);
                     }
                 } else {
                     const float a0 = bf16_lo(v.x), a1 = bf16_hi(v.x), a2 = bf16_lo(v.y);
@@ -303,9 +314,7 @@ __device__ void square_sum(const Pipe &p, It it, int row, int lane)
                     ss2 = fmaf(a6, a6, ss2); ss3 = fmaf(a7, a7, ss3);
                 }
             }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&p.empty[stage]);
-            if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
+            if constexpr (!kFp8) release();
         }
         if (!ok) break;
         // hand the segment's row sums to the epilogue

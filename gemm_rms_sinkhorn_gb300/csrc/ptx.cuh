@@ -291,14 +291,17 @@ __device__ __forceinline__ void st_stream_v4(void *p, uint4 v)
 
 // bf16 <-> fp32 on packed pairs.  Widening is exact (bf16 is the top half of
 // binary32); narrowing rounds to nearest even.
-// Two e4m3 codes (bits 0-7 and 8-15 of w) to fp32: exact (e4m3 is a subset of f16).
-__device__ __forceinline__ void e4m3x2_to_f32(uint32_t w, float &lo, float &hi)
+// Squares of two e4m3 codes (bits 0-7 and 8-15 of w) added to lo and hi.  The
+// codes widen to f16 exactly (e4m3 is a subset of f16) and the mixed-precision
+// fma takes f16 factors with an fp32 addend, so each step equals
+// fmaf(x, x, acc) on the fp32 value x: one rounding, no separate conversion.
+__device__ __forceinline__ void e4m3x2_square_add(uint32_t w, float &lo, float &hi)
 {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(w & 0xFFFFu)));
     asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "cvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi) : "r"(h2));
+        "fma.rn.f32.f16 %0, a, a, %0;\n\tfma.rn.f32.f16 %1, b, b, %1;\n\t}"
+        : "+f"(lo), "+f"(hi) : "r"(h2));
 }
 
 // Two fp32 to e4m3 codes (lo in bits 0-7): round to nearest even, saturating
