@@ -22,10 +22,12 @@
 //   pairs    with 256-column tiles and enough of them, clusters of two CTAs
 //            share each B box by multicast (see "CTA pairs" below);
 //   256 rows with 256-column tiles, long K and enough of them, a CTA takes
-//            256 × 256 tiles (see "256-row tiles" below).
-// The square sums of a row tile are computed once per run of its tiles in a
-// CTA, not once per column tile as on the page: the CUDA-core work is cheap,
-// but its shared-memory reads compete with the tensor cores' operand reads.
+//            256 × 256 tiles in a grouped order that keeps the GPU on a few
+//            row tiles at a time (see "256-row tiles" below).
+// In the 128-row kernels the square sums of a row tile are computed once per
+// run of its tiles in a CTA, not once per column tile as on the page: the
+// CUDA-core work is cheap, but its shared-memory reads compete with the
+// tensor cores' operand reads.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -539,6 +541,17 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 // the ring's bytes against L2 latency are what bound the 128-row kernel.  The
 // accumulators are single-buffered: the epilogue frees the first as soon as it
 // has read it, so the next tile's first MMAs overlap the second half.
+//
+// Tile order: groups of kGroup2 row tiles, column-major inside a group, dealt
+// round-robin over the CTAs, so the 152 tiles in flight at any time span about
+// kGroup2 + 2 row tiles (at K = 4096, 20 MB of A) next to the B boxes, which
+// stay in L2.  A CTA's consecutive tiles then sit in different row tiles, so
+// each tile computes its own square sums (the A stages are in shared memory
+// anyway).  Measured against contiguous runs of one row tile per CTA, whose
+// 64 concurrent row tiles (128 MB of A at 16384 × 4096) overflow L2: 353 ->
+// 336 us at M, K, N = 16384, 4096, 4096 and 1600 -> 1346 us at 32768, 4096,
+// 8192, with bitwise equal results.
+constexpr int kGroup2 = 8;
 constexpr int kBM2 = 2 * kBM;
 constexpr int kBoxA2 = kBM2 * kBK * 2;           // 32 KB
 constexpr int kBoxB2 = 256 * kBK * 2;            // 32 KB
@@ -549,17 +562,23 @@ constexpr int kBar2Bytes = 256;
 constexpr int kSmem2 = 1024 + kStages2 * kStage2 + kSs2Bytes + kBar2Bytes;
 static_assert(kSmem2 <= 227 * 1024, "shared memory");
 
-// Whole 256 × 256 tiles of a CTA, row tiles outermost.
+// The whole 256 × 256 tiles of a CTA: tile indices t = cta, cta + grid, ...
+// below `end`, each mapped to (row tile, column tile) by the grouped order.
 struct TIter {
     int64_t t, end;
-    int n_tiles;
+    int n_tiles, stride, m_tiles;
     __device__ bool next(Segment &s) {
         if (t >= end) return false;
-        s.m = static_cast<int>(t / n_tiles);
-        s.n = static_cast<int>(t - static_cast<int64_t>(s.m) * n_tiles);
+        const int64_t per_group = static_cast<int64_t>(kGroup2) * n_tiles;
+        const int g = static_cast<int>(t / per_group);
+        const int w = static_cast<int>(t - static_cast<int64_t>(g) * per_group);
+        const int left = m_tiles - g * kGroup2;  // row tiles in this group
+        const int rows = left < kGroup2 ? left : kGroup2;
+        s.m = g * kGroup2 + w % rows;
+        s.n = w / rows;
         s.k0 = 0;
         s.k1 = 0;  // unused: every tile runs all K blocks
-        ++t;
+        t += stride;
         return true;
     }
 };
@@ -576,7 +595,7 @@ struct M2Bars {
 __device__ void m2_producer(const pipe::Pipe &p, const M2Bars &b, TIter it, int kbt,
                             const CUtensorMap *tm_a, const CUtensorMap *tm_b)
 {
-    const uint64_t pol_a = ptx::policy_evict_normal();  // re-read by the next column tiles
+    const uint64_t pol_a = ptx::policy_evict_normal();  // read by the group's other column tiles
     const uint64_t pol_b = ptx::policy_evict_last();    // re-read by every row tile
     int stage = 0;
     uint32_t phase = 0;
@@ -658,7 +677,7 @@ __device__ void m2_mma_issuer(const pipe::Pipe &p, const M2Bars &b, TIter it, in
 
 
 // Thread t sums rows t and t + 128 of the tile; a tile of the previous tile's
-// row tile reuses its sums (see row_square_sums).
+// row tile (rare in the grouped order) reuses its sums.
 __device__ void m2_square_sums(const pipe::Pipe &p, const M2Bars &b, TIter it, int kbt, int t,
                                int lane)
 {
@@ -762,7 +781,8 @@ rmsnorm_gemm_m256_kernel(const __grid_constant__ CUtensorMap tm_a,
     p.tmem_base = *b.tmem_holder;
     ptx::pdl_wait();
 
-    const TIter segs{tiles * cta / gridDim.x, tiles * (cta + 1) / gridDim.x, n_tiles};
+    const TIter segs{cta, tiles, n_tiles, static_cast<int>(gridDim.x),
+                     static_cast<int>(tiles / n_tiles)};
     const float inv_k = 1.0f / static_cast<float>(K);
 
     if (warp == 0) {
