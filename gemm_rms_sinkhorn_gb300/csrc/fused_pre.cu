@@ -72,8 +72,13 @@ template <int n>
 struct FCfg {
     static constexpr int N = n * n + 2 * n;
     static constexpr int NPAD = (N + 15) / 16 * 16;
-    static constexpr int kRingBudget = n <= 4 ? 124 * 1024 : 134 * 1024;
-    static constexpr int kSlots = n <= 4 ? 10 : 8;  // X re-read slots (shared memory left over)
+    // n <= 4: a 4-stage GEMM ring and 15 re-read slots.  The producer is held
+    // back by LeadIter anyway, and the re-read is the latency-bound side:
+    // measured at B=16384, C=7168, 6 stages and 10 slots took 663.5 us per
+    // forward, 5 and 12 took 660.1, 4 and 15 took 656.6 (at B=4096, C=4096:
+    // 107.2, 106.6, 106.2 us).
+    static constexpr int kRingBudget = n <= 4 ? 84 * 1024 : 134 * 1024;
+    static constexpr int kSlots = n <= 4 ? 15 : 8;  // X re-read slots (shared memory left over)
     // n <= 4: the epilogue stages its partial in shared memory and stores it
     // coalesced; wider rows do not fit and are stored from registers
     static constexpr bool kStage = n <= 4;
