@@ -35,6 +35,24 @@ def test_kernel_bytes_prefill():
     assert k["post_res_apply"] == 2_115_239_936
 
 
+def test_kernel_bytes_precision_variants():
+    """The same accounting for the fp8 chain (every activation and weight value one
+    byte) and the fp32-weight chain (φ as 2N bf16 rows, F_out fp32), written out."""
+    B, n, C = 16384, 4, 7168
+    K, N = n * C, n * n + 2 * n
+    yr = 4 * B * N + 4 * B                   # Y and r, fp32
+    coef = yr + 4 * N + 4 * B * (2 * n + n * n)  # Y, r, b read; H written
+    hpre, hres_post = 4 * B * n, 4 * B * n * n + 4 * B * n
+    e = bench.kernel_bytes(B, n, C, "e4m3")
+    assert e["gemm_rms"] == B * K + N * K + yr + coef - yr == 473_661_536
+    assert e["pre_apply"] == B * K + hpre + B * C == 587_464_704
+    assert e["post_res_apply"] == 2 * B * K + B * C + hres_post == 1_058_275_328
+    f = bench.kernel_bytes(B, n, C, "f32w")
+    assert f["gemm_rms"] == 2 * B * K + 2 * (2 * N) * K + coef == 945_487_968
+    assert f["pre_apply"] == 2 * B * K + hpre + 2 * B * C == 1_174_667_264
+    assert f["post_res_apply"] == 4 * B * K + 4 * B * C + hres_post == 2_350_120_960
+
+
 def test_tokens_per_second_is_whole_job():
     assert bench.tokens_per_second(16384, 4, 10, 1000.0) == 16384 * 4 * 10
     assert bench.max_over_ranks(3.5) == 3.5
