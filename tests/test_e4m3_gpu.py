@@ -106,7 +106,10 @@ def test_pre_apply_e4m3_one_hot_reproduces_every_code():
         assert np.array_equal(got[~zero], want[~zero]) and np.all(dec(got[zero]) == 0)
 
 
-@pytest.mark.parametrize("B,n,C", [(64, 4, 256), (7, 1, 16), (300, 8, 512), (129, 3, 4096)])
+# every n from 1 to 8 (each is its own instantiation of the three e4m3 kernels),
+# ragged token tiles, C a multiple of 16 but not of 64
+@pytest.mark.parametrize("B,n,C", [(64, 4, 256), (7, 1, 16), (300, 8, 512), (129, 3, 4096),
+                                   (200, 2, 256), (65, 5, 272), (129, 6, 48), (257, 7, 16)])
 def test_forward_e4m3_matches_oracle(B, n, C):
     X, P, Fo, bias = inputs(B, n, C, seed=82)
     out = mhc.alloc_outputs(B, n, C)
