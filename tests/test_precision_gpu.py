@@ -133,3 +133,11 @@ def test_forward_f32w_chain_every_n(n):
     the coefficients in its finalize: one GEMM width per n (2N padded to 16)."""
     wl = WORKLOADS["tiny"].with_(B=3200, n=n, C=64, bias_std=0.3)
     forward_f32w(wl, seed=77 + n, rows=sample_rows(wl.B, 64))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 6, 7])
+def test_forward_f32w_decode_every_n(n):
+    """Up to 3072 tokens the forward takes the one-launch small-batch path with the
+    split weight (its partial rows hold both halves of each column pair): every n."""
+    wl = WORKLOADS["tiny"].with_(B=100, n=n, C=72, bias_std=0.3)
+    forward_f32w(wl, seed=90 + n)
