@@ -46,6 +46,10 @@ KERNELS = ("gemm_rms", "pre_apply", "post_res_apply")
 # kernel -> source file whose contents the stored DRAM counters were taken from
 KERNEL_SOURCES = {"gemm_rms": "gemm_rms.cu", "pre_apply": "apply.cu",
                   "post_res_apply": "apply.cu"}
+# Kernels one prefill forward step launches (the chain, far above the small-batch
+# threshold of 3072 tokens): zero_tickets_kernel (the split-K tile counters of the
+# caller's workspace), gemm_rms_kernel, pre_apply_kernel and post_res_apply_kernel.
+LAUNCHES_PER_STEP = 4
 
 
 def algorithmic_bytes(B: int, n: int, C: int, precision: str = "bf16") -> dict:
@@ -678,7 +682,7 @@ def main() -> int:
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "link_copy_ms_per_step": link_ms,
                 "link_frac": link_ms / e2e_ms if e2e_ms > 0 else None},
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
     }
