@@ -78,6 +78,7 @@ _SIGS = {
                                             _i32, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                             _sz, _vp, ctypes.c_uint64], _i32),
     "mhc_testing_recip": ([_vp, _vp, _i64, _vp], _i32),
+    "mhc_testing_host_chunks": ([_i64, _vp, _i64, ctypes.POINTER(_i64)], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -254,6 +255,17 @@ def mhc_testing_recip(x, out, stream=None):
     f = torch.float32
     _check(_lib.mhc_testing_recip(_ptr(x, f, "x"), _ptr(out, f, "out"), x.numel(),
                                   _stream(stream)), "mhc_testing_recip")
+
+
+def mhc_testing_host_chunks(B: int) -> list:
+    """Token counts of the chunks mhc_forward_host cuts a batch of B tokens into."""
+    count = ctypes.c_int64(0)
+    _check(_lib.mhc_testing_host_chunks(B, None, 0, ctypes.byref(count)),
+           "mhc_testing_host_chunks")
+    sizes = (ctypes.c_int64 * max(count.value, 1))()
+    _check(_lib.mhc_testing_host_chunks(B, sizes, count.value, ctypes.byref(count)),
+           "mhc_testing_host_chunks")
+    return list(sizes[:count.value])
 
 
 def mhc_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B, n, C,

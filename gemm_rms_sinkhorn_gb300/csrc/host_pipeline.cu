@@ -21,7 +21,9 @@
 #include <mutex>
 #include <vector>
 
+#include "mhc.h"
 #include "mhc_internal.h"
+#include "mhc_testing.h"
 
 namespace mhc {
 namespace {
@@ -60,10 +62,11 @@ cudaError_t init_runtime(HostRuntime &rt)
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
-// Token count of each chunk, in order.  The first copy in and the last copy
-// out overlap nothing, so the schedule ramps up (256, 512, then full chunks)
-// and back down (512, 256) at the end; a batch too small for the ramp goes in
-// equal chunks of at most 256 tokens.
+// Token count of each chunk, in order, for chunks of at most `full` tokens.
+// The first copy in and the last copy out overlap nothing, so the schedule
+// ramps up (full/4, full/2, then full chunks) and back down (full/2, full/4)
+// at the end; a batch too small for the ramp goes in equal chunks of full/4
+// tokens (at least 1), the last possibly shorter.
 std::vector<int64_t> chunk_sizes(int64_t B, int64_t full)
 {
     const int64_t ramp[2] = {full / 4, full / 2};
@@ -207,3 +210,15 @@ cudaError_t run_forward_host(const uint16_t *X, const uint16_t *phi_t, const uin
 }
 
 }  // namespace mhc
+
+extern "C" int mhc_testing_host_chunks(int64_t B, int64_t *sizes, int64_t capacity,
+                                       int64_t *count)
+{
+    if (B < 0 || count == nullptr || capacity < 0 || (capacity > 0 && sizes == nullptr))
+        return MHC_ERR_INVALID;
+    const std::vector<int64_t> plan =
+        mhc::chunk_sizes(B, B < mhc::kHostChunkTokens ? B : mhc::kHostChunkTokens);
+    *count = static_cast<int64_t>(plan.size());
+    for (int64_t i = 0; i < *count && i < capacity; ++i) sizes[i] = plan[i];
+    return MHC_OK;
+}

@@ -190,8 +190,9 @@ size_t mhc_forward_host_scratch_bytes(int64_t B, int n, int64_t C);
  * The batch goes through the device in chunks of tokens: 256 and 512 first,
  * then chunks of 1024 (the last of them possibly shorter), then 512 and 256,
  * so that the first copy in and the last copy out, which nothing overlaps,
- * are short; a batch below 2560 tokens goes in chunks of 256 (the last
- * possibly shorter).  The copy of one chunk to the device, the forward of the
+ * are short; a batch below 2560 tokens goes in chunks of 256 (of a quarter
+ * of the batch, at least 1, below 1024 tokens), the last possibly shorter.
+ * mhc_testing_host_chunks (mhc_testing.h) returns the plan.  The copy of one chunk to the device, the forward of the
  * previous one (mhc_forward's path for the chunk size) and the copy of the
  * outputs before that back to the host run concurrently on two internal copy
  * streams and `stream`.  Every copy is one cudaMemcpyAsync.  Results equal

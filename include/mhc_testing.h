@@ -102,6 +102,15 @@ int mhc_testing_forward_decode_stalled(const mhc_bf16 *X, const mhc_bf16 *phi_t,
  */
 int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t stream);
 
+/*
+ * The chunk plan of mhc_forward_host for a batch of B tokens (host only, no
+ * device needed): *count = the number of chunks, and the first
+ * min(*count, capacity) token counts, in order, go to sizes[] (host memory).
+ * MHC_ERR_INVALID for B < 0, capacity < 0, a NULL count, or a NULL sizes
+ * with capacity > 0.
+ */
+int mhc_testing_host_chunks(int64_t B, int64_t *sizes, int64_t capacity, int64_t *count);
+
 #ifdef __cplusplus
 }
 #endif

@@ -2,6 +2,7 @@
 include/mhc.h declares, and rejects bad arguments on the host before any
 device work.  Pointers here are fake addresses that are never dereferenced.
 """
+import ctypes
 import os
 import re
 import subprocess
@@ -228,3 +229,32 @@ def test_e4m3_calls_validate_on_the_host():
     assert L.mhc_gemm_rms_e4m3(A, B_, 4, 4, 32, C_, D, W, 1 << 30, None) == NO_DEVICE
     assert L.mhc_post_res_apply_e4m3(A, B_, C_, D, 4, 4, 32, A, None) == NO_DEVICE  # in place
     assert L.mhc_post_res_apply_e4m3(A, B_, C_, D, 4, 4, 32, A + 16, None) == mhc.MHC_ERR_INVALID
+
+
+@pytest.mark.parametrize("B", [1, 2, 3, 7, 100, 1000, 1023, 1024, 2000, 2559, 2560, 2561,
+                               4100, 16384, 100000])
+def test_host_chunk_plan(B):
+    """mhc_forward_host's chunks (host logic, no device): they cover the batch in
+    order, none exceeds 1024 tokens, large batches ramp 256, 512 up and 512, 256
+    down around full chunks, and small ones go in equal chunks."""
+    c = mhc.mhc_testing_host_chunks(B)
+    assert sum(c) == B and all(v > 0 for v in c) and max(c) <= 1024
+    if B >= 2560:
+        assert c[:2] == [256, 512] and c[-2:] == [512, 256]
+        mid = c[2:-2]
+        assert all(v == 1024 for v in mid[:-1]) and 0 < mid[-1] <= 1024
+    else:
+        step = max(min(B, 1024) // 4, 1)
+        assert all(v == step for v in c[:-1]) and 0 < c[-1] <= step
+
+
+def test_host_chunk_plan_rules():
+    count = ctypes.c_int64(-1)
+    f = L.mhc_testing_host_chunks
+    assert f(0, None, 0, ctypes.byref(count)) == mhc.MHC_OK and count.value == 0
+    assert f(-1, None, 0, ctypes.byref(count)) == mhc.MHC_ERR_INVALID
+    assert f(10, None, 0, None) == mhc.MHC_ERR_INVALID
+    assert f(10, None, 4, ctypes.byref(count)) == mhc.MHC_ERR_INVALID
+    sizes = (ctypes.c_int64 * 2)()
+    assert f(16384, sizes, 2, ctypes.byref(count)) == mhc.MHC_OK  # capacity below the count
+    assert count.value == 19 and list(sizes) == [256, 512]
