@@ -1,6 +1,10 @@
 """The C ABI without a GPU: the library loads, exports every call that
 include/mhc.h declares, and rejects bad arguments on the host before any
-device work.  Pointers here are fake addresses that are never dereferenced.
+device work.  Pointers here are fake addresses that are never dereferenced
+on a machine without a GPU: calls whose arguments pass every host check stop
+at the device check there.  On a machine with a GPU those calls would launch
+kernels on the fake addresses, so every test that passes them is skipped
+wherever a CUDA device is visible (`no_gpu`).
 """
 import ctypes
 import os
@@ -16,6 +20,11 @@ HEADERS = sorted(os.path.join(ROOT, "include", h) for h in os.listdir(os.path.jo
 
 mhc = pytest.importorskip("gemm_rms_sinkhorn_gb300")
 L = mhc._lib
+
+import torch  # noqa: E402  (the binding has imported it already)
+
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(),
+                            reason="fake device addresses: only where no GPU is visible")
 
 
 def declared_functions():
@@ -86,6 +95,7 @@ def fwd(X=A, phi=B_, Fo=C_, bias=D, iters=20, Bt=4, n=4, C=256, Y=E, r=F, hp=G, 
 NO_DEVICE = mhc.MHC_ERR_CUDA  # valid host arguments reach the device check
 
 
+@no_gpu
 def test_empty_batch_is_a_noop():
     assert gemm(Bt=0, X=None, phi=None, Y=None, r=None, ws=None, wsb=0) == mhc.MHC_OK
     assert coeffs(Bt=0) == mhc.MHC_OK
@@ -95,6 +105,7 @@ def test_empty_batch_is_a_noop():
     assert fwd(Bt=0) == mhc.MHC_OK
 
 
+@no_gpu
 @pytest.mark.parametrize("call", [gemm, gemm_coeffs, pre, post, fwd])
 def test_shape_rules(call):
     assert call(n=0) == mhc.MHC_ERR_UNSUPPORTED
@@ -105,6 +116,7 @@ def test_shape_rules(call):
     assert call(Bt=1 << 31) == mhc.MHC_ERR_UNSUPPORTED  # token rows are 32-bit TMA coordinates
 
 
+@no_gpu
 def test_coeffs_rules():
     assert coeffs(n=9) == mhc.MHC_ERR_UNSUPPORTED
     assert coeffs(iters=-1) == mhc.MHC_ERR_INVALID
@@ -118,6 +130,7 @@ def test_coeffs_rules():
     assert coeffs(Y=None) == mhc.MHC_ERR_INVALID
 
 
+@no_gpu
 def test_null_and_alignment():
     assert gemm(X=None) == mhc.MHC_ERR_INVALID
     assert pre(Fp=None) == mhc.MHC_ERR_INVALID
@@ -128,6 +141,7 @@ def test_null_and_alignment():
     assert coeffs(hr=F + 4) == mhc.MHC_ERR_ALIGN
 
 
+@no_gpu
 def test_overlap_rules():
     # an output over an input
     assert gemm(Y=A + 64) == mhc.MHC_ERR_INVALID
@@ -141,6 +155,7 @@ def test_overlap_rules():
     assert fwd(Fp=A) == mhc.MHC_ERR_INVALID
 
 
+@no_gpu
 def test_valid_arguments_reach_the_device_check():
     assert gemm() == NO_DEVICE
     assert coeffs() == NO_DEVICE
@@ -163,6 +178,7 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     assert res.returncode != 0 and "ImportError" in res.stderr
 
 
+@no_gpu
 def test_testing_hooks_validate_on_the_host():
     assert L.mhc_testing_recip(A, B_, -1, None) == mhc.MHC_ERR_INVALID
     assert L.mhc_testing_recip(A, B_, 0, None) == mhc.MHC_OK
@@ -184,6 +200,7 @@ def test_testing_hooks_validate_on_the_host():
     assert L.mhc_testing_forward_decode_stalled(*args) == mhc.MHC_ERR_INVALID
 
 
+@no_gpu
 def test_forward_host_validates_on_the_host():
     f = L.mhc_forward_host
     args = [A, B_, C_, 0.01, 0.01, 0.01, D, 20, 4, 4, 256, E, F, G, H, I, J, 0x1_0000_0000, W,
@@ -206,6 +223,7 @@ def test_forward_host_validates_on_the_host():
     assert mhc._lib.mhc_forward_host_scratch_bytes(64, 4, 256) == 0  # needs a device
 
 
+@no_gpu
 def test_rmsnorm_gemm_validates_on_the_host():
     f = L.mhc_rmsnorm_gemm
     assert f(A, B_, 0, 64, 64, 1e-5, C_, None, 0, None) == mhc.MHC_OK  # empty
@@ -223,6 +241,7 @@ def test_rmsnorm_gemm_validates_on_the_host():
     assert mhc._lib.mhc_rmsnorm_gemm_workspace_bytes(16, 64, 64) == 0  # needs a device
 
 
+@no_gpu
 def test_e4m3_calls_validate_on_the_host():
     assert L.mhc_pre_apply_e4m3(A, B_, 4, 4, 24, C_, None) == mhc.MHC_ERR_UNSUPPORTED  # C % 16
     assert L.mhc_pre_apply_e4m3(A, B_, 4, 4, 32, C_, None) == NO_DEVICE
