@@ -34,6 +34,8 @@ MHC_ERR_CUDA = -4
 MHC_ERR_TIMEOUT = -5
 MHC_ERR_WORKSPACE = -6
 
+MHC_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/mhc.h: the built-in scratch of mhc_gemm_rms_noalloc
+
 _vp, _i64, _i32, _f32, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
                               ctypes.c_size_t)
 _SIGS = {
@@ -79,6 +81,7 @@ _SIGS = {
                                             _sz, _vp, ctypes.c_uint64], _i32),
     "mhc_testing_recip": ([_vp, _vp, _i64, _vp], _i32),
     "mhc_testing_host_chunks": ([_i64, _vp, _i64, ctypes.POINTER(_i64)], _i32),
+    "mhc_testing_memory_checks": ([_i32], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)

@@ -4,6 +4,7 @@
 // nothing here allocates device memory.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
 
@@ -104,9 +105,32 @@ int check_overlap(const Buf *outs, int n_out, const Buf *ins, int n_in, const vo
     return MHC_OK;
 }
 
-// Where each pointer lives: host memory (page-locked or pageable) or device
-// memory, as the runtime records it.  MHC_ERR_INVALID on a mismatch.
-int check_memory_kind(const Buf *bufs, int count, bool host)
+// Whether the pointer checks of the device-memory entry points run (on unless a
+// test turns them off to time their cost).
+std::atomic<int> g_memory_checks{1};
+
+// Every buffer must be device memory of the current device (cudaMalloc,
+// stream-ordered pools or mapped VMM ranges): a host pointer, managed memory
+// or another GPU's memory reached over peer access is MHC_ERR_INVALID, before
+// anything is launched.  The kernels' TMA descriptors and stores assume local
+// device memory.
+int check_on_device(const Buf *bufs, int count, const DeviceInfo &info)
+{
+    if (!g_memory_checks.load(std::memory_order_relaxed)) return MHC_OK;
+    for (int i = 0; i < count; ++i) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, bufs[i].p) != cudaSuccess) {
+            cudaGetLastError();  // not sticky; clear it
+            return MHC_ERR_INVALID;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != info.device) return MHC_ERR_INVALID;
+    }
+    return MHC_OK;
+}
+
+// Every buffer must be host memory (page-locked or pageable), as the runtime
+// records it: device or managed memory is MHC_ERR_INVALID.
+int check_on_host(const Buf *bufs, int count)
 {
     for (int i = 0; i < count; ++i) {
         cudaPointerAttributes a{};
@@ -114,9 +138,8 @@ int check_memory_kind(const Buf *bufs, int count, bool host)
             cudaGetLastError();  // not sticky; clear it
             return MHC_ERR_INVALID;
         }
-        const bool is_host = a.type == cudaMemoryTypeHost || a.type == cudaMemoryTypeUnregistered;
-        const bool is_dev = a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-        if (host ? !is_host : !is_dev) return MHC_ERR_INVALID;
+        if (a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeUnregistered)
+            return MHC_ERR_INVALID;
     }
     return MHC_OK;
 }
@@ -252,11 +275,14 @@ static int forward_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_b
     MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 7, info));
     const size_t need = forward_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[7].bytes = need;
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    MHC_TRY(check_on_device(outs + 7, 1, info));
     if (path == Path::Fused && !fused_pre_eligible(B, n, C, info.num_sms))
         return MHC_ERR_UNSUPPORTED;
     if ((path == Path::Decode || path == Path::DecodeStalled) && !decode_pre_eligible(B, n, C))
@@ -283,11 +309,14 @@ static int gemm_rms_checked(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B,
     MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 2, info));
     const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[2].bytes = need;
     MHC_TRY(check_ptrs(outs + 2, 1));
     MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    MHC_TRY(check_on_device(outs + 2, 1, info));
     return cuda_status(launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
                                        reinterpret_cast<cudaStream_t>(stream), wait_limit_ns,
                                        stall_stage));
@@ -352,6 +381,8 @@ int mhc_coeffs(const float *Y, const float *r, float alpha_pre, float alpha_post
     MHC_TRY(check_overlap(outs, 3, ins, 3, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 3, info));
+    MHC_TRY(check_on_device(outs, 3, info));
     return cuda_status(launch_coeffs(Y, r, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
                                      H_pre, H_post, H_res, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -377,11 +408,14 @@ int mhc_gemm_rms_coeffs(const mhc_bf16 *X, const mhc_bf16 *phi_t, float alpha_pr
     MHC_TRY(check_overlap(outs, 5, ins, 3, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 3, info));
+    MHC_TRY(check_on_device(outs, 5, info));
     const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[5].bytes = need;
     MHC_TRY(check_ptrs(outs + 5, 1));
     MHC_TRY(check_overlap(outs, 6, ins, 3, nullptr, nullptr));
+    MHC_TRY(check_on_device(outs + 5, 1, info));
     return cuda_status(launch_gemm_rms(
         X, phi_t, B, n, C, Y, r, workspace, info.num_sms, reinterpret_cast<cudaStream_t>(stream),
         kWaitLimitNs, -1,
@@ -400,6 +434,8 @@ int mhc_pre_apply(const mhc_bf16 *X, const float *H_pre, int64_t B, int n, int64
     MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(
         launch_pre_apply(X, H_pre, B, n, C, F_pre, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -418,6 +454,8 @@ int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_
     MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_post_res_apply(X, F_out, H_res, H_post, B, n, C, X_next,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -480,6 +518,8 @@ int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t s
     MHC_TRY(check_overlap(outs, 1, ins, 1, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 1, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_recip(in, out, count, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -497,6 +537,8 @@ int mhc_split_phi(const float *phi_t, int n, int64_t C, mhc_bf16 *phi_split, mhc
     MHC_TRY(check_overlap(outs, 1, ins, 1, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 1, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_split_phi(phi_t, n, C, phi_split,
                                         reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -516,11 +558,14 @@ int mhc_gemm_rms_split(const mhc_bf16 *X, const mhc_bf16 *phi_split, int64_t B, 
     MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 2, info));
     const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[2].bytes = need;
     MHC_TRY(check_ptrs(outs + 2, 1));
     MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    MHC_TRY(check_on_device(outs + 2, 1, info));
     return cuda_status(launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -540,6 +585,8 @@ int mhc_post_res_apply_f32(const mhc_bf16 *X, const float *F_out, const float *H
     MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next,
                                                  reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -566,11 +613,14 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
     MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 7, info));
     const size_t need = forward_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[7].bytes = need;
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    MHC_TRY(check_on_device(outs + 7, 1, info));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C)) {
@@ -612,11 +662,14 @@ int mhc_gemm_rms_e4m3(const uint8_t *X, const uint8_t *phi_t, int64_t B, int n, 
     MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 2, info));
     const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[2].bytes = need;
     MHC_TRY(check_ptrs(outs + 2, 1));
     MHC_TRY(check_overlap(outs, 3, ins, 2, nullptr, nullptr));
+    MHC_TRY(check_on_device(outs + 2, 1, info));
     return cuda_status(launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms,
                                             reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -634,6 +687,8 @@ int mhc_pre_apply_e4m3(const uint8_t *X, const float *H_pre, int64_t B, int n, i
     MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_pre_apply_e4m3(X, H_pre, B, n, C, F_pre,
                                              reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -653,6 +708,8 @@ int mhc_post_res_apply_e4m3(const uint8_t *X, const uint8_t *F_out, const float 
     MHC_TRY(check_overlap(outs, 1, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     return cuda_status(launch_post_res_apply_e4m3(X, F_out, H_res, H_post, B, n, C, X_next,
                                                   reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -679,11 +736,14 @@ int mhc_forward_e4m3(const uint8_t *X, const uint8_t *phi_t, const uint8_t *F_ou
     MHC_TRY(check_overlap(outs, 7, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 4, info));
+    MHC_TRY(check_on_device(outs, 7, info));
     const size_t need = gemm_rms_workspace_bytes(B, n, C, info.num_sms);
     if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
     outs[7].bytes = need;
     MHC_TRY(check_ptrs(outs + 7, 1));
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
+    MHC_TRY(check_on_device(outs + 7, 1, info));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = launch_gemm_rms_e4m3(X, phi_t, B, n, C, Y, r, workspace, info.num_sms, s,
                                          coef_args(alpha_pre, alpha_post, alpha_res, bias, iters,
@@ -725,12 +785,15 @@ int mhc_rmsnorm_gemm(const mhc_bf16 *A, const mhc_bf16 *B_t, int64_t M, int64_t 
     MHC_TRY(check_overlap(outs, 1, ins, 2, nullptr, nullptr));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
+    MHC_TRY(check_on_device(ins, 2, info));
+    MHC_TRY(check_on_device(outs, 1, info));
     const size_t need = rmsnorm_gemm_workspace_bytes(M, K, N, info.num_sms);
     if (need > 0) {
         if (workspace == nullptr || workspace_bytes < need) return MHC_ERR_WORKSPACE;
         outs[1].bytes = need;
         MHC_TRY(check_ptrs(outs + 1, 1));
         MHC_TRY(check_overlap(outs, 2, ins, 2, nullptr, nullptr));
+        MHC_TRY(check_on_device(outs + 1, 1, info));
     }
     return cuda_status(launch_rmsnorm_gemm(A, B_t, M, K, N, eps, C, need > 0 ? workspace : nullptr,
                                            info.num_sms, reinterpret_cast<cudaStream_t>(stream)));
@@ -767,15 +830,20 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
     MHC_TRY(check_overlap(outs, 8, ins, 4, X_next, X));
     DeviceInfo info;
     MHC_TRY(check_device(&info));
-    MHC_TRY(check_memory_kind(host_in, 2, true));
-    MHC_TRY(check_memory_kind(outs, 7, true));
-    MHC_TRY(check_memory_kind(dev_in, 2, false));
-    MHC_TRY(check_memory_kind(outs + 7, 1, false));
+    MHC_TRY(check_on_host(host_in, 2));
+    MHC_TRY(check_on_host(outs, 7));
+    MHC_TRY(check_on_device(dev_in, 2, info));
+    MHC_TRY(check_on_device(outs + 7, 1, info));
     if (scratch_bytes < host_chunk_layout(B, n, C, info.num_sms).total) return MHC_ERR_WORKSPACE;
     return cuda_status(run_forward_host(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias,
                                         iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre,
                                         X_next, scratch, info.num_sms,
                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int mhc_testing_memory_checks(int on)
+{
+    return g_memory_checks.exchange(on != 0 ? 1 : 0);
 }
 
 int mhc_device_status(int *status)

@@ -8,7 +8,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "mhc.h"
 
@@ -18,24 +17,22 @@ constexpr size_t kScratchBytes = MHC_NOALLOC_SCRATCH_BYTES;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device.  The name is
-// only a host-side stand-in in host code, so the address is looked up once
-// per device with that device current, and cached.  Returns nullptr when the
-// lookup fails.
+// Device address of g_noalloc_scratch in the current context.  In host code
+// the array's name is only a host-side stand-in, so the address is looked up
+// with the caller's device current, on every call: the lookup allocates
+// nothing, and a context created anew (after cudaDeviceReset, say) may hold
+// the array at another address, so no address is kept between calls.  The
+// first lookup on a device loads the library's device code there, which is why
+// the first call on a device should come before any stream capture.  Returns
+// nullptr when the lookup fails.
 void *current_device_scratch()
 {
-    constexpr int kMaxDevices = 64;
-    static void *addr[kMaxDevices] = {};
-    static std::mutex mu;
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-        addr[dev] = p;
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) {
+        cudaGetLastError();  // not sticky; clear it
+        return nullptr;
     }
-    return addr[dev];
+    return p;
 }
 
 }  // namespace

@@ -19,8 +19,6 @@
 //            to finish a tile adds the partials in contributor order;
 //   epilogue the accumulator leaves TMEM 32 columns at a time, is scaled by
 //            rstd, rounded to bf16 (RNE) and stored;
-//   pairs    with 256-column tiles and enough of them, clusters of two CTAs
-//            share each B box by multicast (see "CTA pairs" below);
 //   256 rows with 256-column tiles, long K and enough of them, a CTA takes
 //            256 × 256 tiles in a grouped order that keeps the GPU on a few
 //            row tiles at a time (see "256-row tiles" below).
@@ -33,7 +31,6 @@
 
 #include <cstdint>
 #include <mutex>
-#include <type_traits>
 
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
@@ -92,177 +89,9 @@ struct RIter {
     }
 };
 
-// ------------------------------------------------------------ CTA pairs
-// With 256-column tiles and whole tiles per CTA, the two CTAs of a cluster
-// take row tiles 2·mp and 2·mp + 1 of the same column tile at the same K
-// blocks: each loads its own A box and half of the B box, multicast into
-// both CTAs' stages, so a CTA reads 32 KB of a 48 KB stage from L2 instead of
-// 48.  Each MMA commit frees the stage in both CTAs (a stage's B half is
-// overwritten by the other CTA's producer).
-
-__device__ __forceinline__ uint32_t cluster_rank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of both CTAs; orders shared-memory and barrier set-up (release)
-// before the other CTA's use of it (acquire).
-__device__ __forceinline__ void cluster_sync()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_inval(uint64_t *bar)
-{
-    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(ptx::smem_u32(bar)) : "memory");
-}
-
-// As ptx::tma_load_2d, written to the same offset in every CTA of `mask`, each
-// CTA's barrier at that offset counting the bytes.
-__device__ __forceinline__ void tma_load_2d_mc(void *smem_dst, const void *tmap, int32_t x,
-                                               int32_t y, uint64_t *bar, uint16_t mask,
-                                               uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(
-            ptx::smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(ptx::smem_u32(bar)),
-        "h"(mask), "l"(policy)
-        : "memory");
-}
-
-// As ptx::mma_commit, arriving on the barrier at the same offset in every CTA of `mask`.
-__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster"
-        ".b64 [%0], %1;" ::"r"(ptx::smem_u32(bar)),
-        "h"(mask)
-        : "memory");
-}
-
-// A pair's whole tiles: pair tile pt is row tiles 2·(pt / n_tiles) + rank of
-// column tile pt % n_tiles.
-struct PIter {
-    int64_t pt, end;
-    int kbt, n_tiles, rank;
-    __device__ bool next(Segment &s) {
-        if (pt >= end) return false;
-        const int64_t mp = pt / n_tiles;
-        s.m = static_cast<int>(2 * mp + rank);
-        s.n = static_cast<int>(pt - mp * n_tiles);
-        s.k0 = 0;
-        s.k1 = kbt;
-        ++pt;
-        return true;
-    }
-};
-
-__device__ __forceinline__ RIter make_segs(const RSched &sch, int cta, std::false_type)
+__device__ __forceinline__ RIter make_segs(const RSched &sch, int cta)
 {
     return RIter{sch.lo(cta), sch.lo(cta + 1), sch.kbt, sch.n_tiles};
-}
-
-// sch counts pair tiles (tiles) and pairs (grid).
-__device__ __forceinline__ PIter make_segs(const RSched &sch, int cta, std::true_type)
-{
-    const int pc = cta >> 1;
-    return PIter{sch.tiles * pc / sch.grid, sch.tiles * (pc + 1) / sch.grid, sch.kbt,
-                 sch.n_tiles, static_cast<int>(cluster_rank())};
-}
-
-// The pair producer: own A box, own half of the B box to both CTAs.  At the
-// end it waits until every stage has been freed by both CTAs' MMAs, so no
-// commit of the other CTA is still on its way to this CTA's barriers.
-template <int NT>
-__device__ void pair_producer(const pipe::Pipe &p, PIter it, const CUtensorMap *tm_a,
-                              const CUtensorMap *tm_b_half)
-{
-    constexpr int kBoxA = pipe::kBoxABytes;
-    constexpr int kHalfRows = NT / 2;
-    const uint64_t pol_a = ptx::policy_evict_normal();  // re-read by the next column tiles
-    const uint64_t pol_b = ptx::policy_evict_last();    // re-read by every pair
-    const int rank = it.rank;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued_mask = 0, issued_parity = 0;
-    Segment sg;
-    bool ok = true;
-    while (ok && it.next(sg)) {
-        for (int kb = sg.k0; kb < sg.k1; ++kb) {
-            if (!pipe::wait(p, &p.empty[stage], phase ^ 1)) {
-                ok = false;
-                break;
-            }
-            uint8_t *a = p.stages + stage * p.stage_bytes;
-            ptx::mbar_arrive_expect_tx(&p.full[stage], p.stage_bytes);  // A and both B halves
-            ptx::tma_load_2d(a, tm_a, kb * kBK, sg.m * kBM, &p.full[stage], pol_a);
-            tma_load_2d_mc(a + kBoxA + rank * kHalfRows * 128, tm_b_half, kb * kBK,
-                           sg.n * NT + rank * kHalfRows, &p.full[stage], 0x3, pol_b);
-            issued_mask |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
-        }
-    }
-    if (ok) {
-        for (int s = 0; s < p.stages_n; ++s) {
-            if (!pipe::wait(p, &p.empty[stage], phase ^ 1)) break;
-            if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
-        }
-    } else {
-        for (int s = 0; s < p.stages_n; ++s) {
-            if (!((issued_mask >> s) & 1u)) continue;
-            volatile int never = 0;
-            ptx::mbar_wait_bounded(&p.full[s], (issued_parity >> s) & 1u, &never, p.limit_ns);
-        }
-    }
-}
-
-// As pipe::mma_issuer for bf16, the stage commits going to both CTAs.
-template <int NT>
-__device__ void pair_mma_issuer(const pipe::Pipe &p, PIter it)
-{
-    constexpr uint32_t idesc = ptx::idesc_bf16_f32(kBM, NT);
-    constexpr int kBoxA = pipe::kBoxABytes;
-    int stage = 0;
-    uint32_t phase = 0;
-    int seg = 0;
-    Segment sg;
-    bool ok = true;
-    while (ok && it.next(sg)) {
-        const int acc = seg & 1;
-        if (!pipe::wait(p, &p.acc_empty[acc], ((seg >> 1) & 1) ^ 1)) break;
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = p.tmem_base + static_cast<uint32_t>(acc * NT);
-        for (int kb = sg.k0; kb < sg.k1; ++kb) {
-            if (!pipe::wait(p, &p.full[stage], phase)) {
-                ok = false;
-                break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t a_addr = ptx::smem_u32(p.stages + stage * p.stage_bytes);
-            const uint64_t a_desc = ptx::smem_desc_sw128(a_addr);
-            const uint64_t b_desc = ptx::smem_desc_sw128(a_addr + kBoxA);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                ptx::mma_bf16(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc,
-                              (kb > sg.k0 || kk > 0) ? 1u : 0u);
-            mma_commit_mc(&p.empty[stage], 0x3);
-            if (++stage == p.stages_n) { stage = 0; phase ^= 1; }
-        }
-        if (!ok) break;
-        ptx::mma_commit(&p.acc_full[acc]);
-        ++seg;
-    }
-    if (!ok || *p.abort) {
-        ptx::mma_commit(p.drain);
-        volatile int never = 0;
-        ptx::mbar_wait_bounded(p.drain, 0, &never, p.limit_ns);
-    }
 }
 
 // Σa² of one 128-byte stage row (64 bf16) into four partial sums.
@@ -341,7 +170,7 @@ __device__ __forceinline__ void store_cols32(const float (&v)[32], float rstd, u
     }
 }
 
-template <int NT, bool kPair>
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1)
 rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const __grid_constant__ CUtensorMap tm_b, int64_t M, int64_t N, int K,
@@ -364,13 +193,6 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
 
     if (threadIdx.x == 0) {
         pipe::init_barriers(p);
-        if constexpr (kPair) {
-            // a stage is freed by both CTAs' MMA commits and this CTA's square sums
-            for (int s2 = 0; s2 < p.stages_n; ++s2) {
-                mbar_inval(&p.empty[s2]);
-                ptx::mbar_init(&p.empty[s2], 2 + 4);
-            }
-        }
         ptx::mbar_init(epi_bar, kEpiThreads);
         *is_last = 0;
         ptx::fence_barrier_init();
@@ -382,31 +204,19 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     if (warp == 1) ptx::tmem_alloc<Cf::kTmemCols>(p.tmem_holder);
     ptx::tc_fence_before();
     __syncwarp();  // whole warps at the (aligned) barrier
-    if constexpr (kPair)
-        cluster_sync();  // both CTAs' barriers exist before either multicasts
-    else
-        __syncthreads();
+    __syncthreads();
     ptx::tc_fence_after();
     p.tmem_base = *p.tmem_holder;
     ptx::pdl_wait();
 
-    const auto segs = make_segs(sch, cta, std::integral_constant<bool, kPair>{});
+    const auto segs = make_segs(sch, cta);
     const float inv_k = 1.0f / static_cast<float>(K);
 
     if (warp == 0) {
-        if (lane == 0) {
-            if constexpr (kPair)
-                pair_producer<NT>(p, segs, &tm_a, &tm_b);
-            else  // A rows are re-read by the next column tiles: keep them in L2
-                pipe::producer<NT>(p, segs, &tm_a, &tm_b, ptx::policy_evict_normal(), -1);
-        }
+        if (lane == 0)  // A rows are re-read by the next column tiles: keep them in L2
+            pipe::producer<NT>(p, segs, &tm_a, &tm_b, ptx::policy_evict_normal(), -1);
     } else if (warp == 1) {
-        if (lane == 0) {
-            if constexpr (kPair)
-                pair_mma_issuer<NT>(p, segs);
-            else
-                pipe::mma_issuer<NT>(p, segs);
-        }
+        if (lane == 0) pipe::mma_issuer<NT>(p, segs);
     } else if (warp < 6) {
         row_square_sums(p, segs, sch.kbt, (warp - 2) * 32 + lane, lane);
     } else {
@@ -522,10 +332,7 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
     // the CTA barrier, which needs whole warps
     __syncwarp();
     ptx::tc_fence_before();
-    if constexpr (kPair)
-        cluster_sync();  // neither CTA leaves while the other may still write to it
-    else
-        __syncthreads();
+    __syncthreads();
     ptx::pdl_trigger();
     if (warp == 1) {
         ptx::tc_fence_after();
@@ -888,8 +695,7 @@ size_t tickets_bytes(int64_t tiles) { return (static_cast<size_t>(tiles) * 4 + 2
 // 256 × 256 tiles when every SM gets at least one and K has at least 64
 // blocks.  Their accumulators are single-buffered, so a tile's epilogue holds
 // up the next tile's first MMAs for a few µs; below 64 K blocks that costs more
-// than the smaller stages gain (measured: K = 4096 and 7168 13–23 % faster than
-// the pairs, K = 1024 and 2048 10–23 % slower).
+// than the smaller stages gain.
 bool m256_ok(int64_t M, int64_t K, int64_t N, int num_sms)
 {
     return tile_cols(N) == 256 && (K + kBK - 1) / kBK >= 64 &&
@@ -918,53 +724,7 @@ cudaError_t launch_m256(const uint16_t *A, const uint16_t *B_t, int64_t M, int64
                       static_cast<int>((N + 255) / 256), C, kWaitLimitNs);
 }
 
-// The CTA-pair schedule: 256-column tiles, pair tiles (two row tiles of one
-// column tile) split in whole pair tiles over num_sms / 2 pairs.  ok = false
-// when there are fewer pair tiles than pairs (the plain schedule then splits K).
-struct PairPlan {
-    bool ok = false;
-    RSched s{};
-};
-
-PairPlan pair_plan(int64_t M, int64_t K, int64_t N, int num_sms)
-{
-    PairPlan pp;
-    if (tile_cols(N) != 256 || num_sms < 2) return pp;
-    RSched &s = pp.s;
-    s.n_tiles = static_cast<int>((N + 255) / 256);
-    const int64_t m_tiles = (M + kBM - 1) / kBM;
-    s.tiles = (m_tiles + 1) / 2 * s.n_tiles;
-    s.kbt = static_cast<int>((K + kBK - 1) / kBK);
-    s.total = s.tiles * s.kbt;
-    s.grid = num_sms / 2;
-    s.aligned = 1;
-    pp.ok = s.tiles >= s.grid;
-    return pp;
-}
-
-// launch_pdl with a cluster of two CTAs along x.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pair(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                        cudaStream_t stream, Args &&...args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
-}
-
-template <int NT, bool kPair>
+template <int NT>
 cudaError_t launch_nt(const CUtensorMap &ta, const CUtensorMap &tb, int64_t M, int64_t N, int K,
                       float eps, const RSched &s, uint16_t *C, int *tickets, float *partials,
                       int device, uint64_t limit, cudaStream_t stream)
@@ -974,20 +734,14 @@ cudaError_t launch_nt(const CUtensorMap &ta, const CUtensorMap &tb, int64_t M, i
     static std::mutex mu;
     if (device < 64 && !((configured >> device) & 1)) {
         std::lock_guard<std::mutex> lock(mu);
-        cudaError_t e = cudaFuncSetAttribute(rmsnorm_gemm_kernel<NT, kPair>,
+        cudaError_t e = cudaFuncSetAttribute(rmsnorm_gemm_kernel<NT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              R::kSmemBytes);
         if (e != cudaSuccess) return e;
         configured |= 1ull << device;
     }
-    if constexpr (kPair)
-        return launch_pair(rmsnorm_gemm_kernel<NT, true>, dim3(2 * s.grid), dim3(kThreads),
-                           R::kSmemBytes, stream, ta, tb, M, N, K, eps, s, C, tickets, partials,
-                           limit);
-    else
-        return launch_pdl(rmsnorm_gemm_kernel<NT, false>, dim3(s.grid), dim3(kThreads),
-                          R::kSmemBytes, stream, ta, tb, M, N, K, eps, s, C, tickets, partials,
-                          limit);
+    return launch_pdl(rmsnorm_gemm_kernel<NT>, dim3(s.grid), dim3(kThreads), R::kSmemBytes,
+                      stream, ta, tb, M, N, K, eps, s, C, tickets, partials, limit);
 }
 
 }  // namespace
@@ -995,7 +749,7 @@ cudaError_t launch_nt(const CUtensorMap &ta, const CUtensorMap &tb, int64_t M, i
 size_t rmsnorm_gemm_workspace_bytes(int64_t M, int64_t K, int64_t N, int num_sms)
 {
     if (M <= 0) return 0;
-    if (m256_ok(M, K, N, num_sms) || pair_plan(M, K, N, num_sms).ok) return 0;
+    if (m256_ok(M, K, N, num_sms)) return 0;
     const RSched s = rng_sched(M, K, N, num_sms);
     if (s.aligned) return 0;
     const size_t slots = static_cast<size_t>(s.grid) + static_cast<size_t>(s.tiles);
@@ -1006,19 +760,10 @@ cudaError_t launch_rmsnorm_gemm(const uint16_t *A, const uint16_t *B_t, int64_t 
                                 int64_t N, float eps, uint16_t *C, void *workspace, int num_sms,
                                 cudaStream_t stream)
 {
-    const PairPlan pp = pair_plan(M, K, N, num_sms);
     int device = 0;
     cudaError_t e;
     if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
     if (m256_ok(M, K, N, num_sms)) return launch_m256(A, B_t, M, K, N, eps, C, num_sms, device, stream);
-    if (pp.ok) {
-        CUtensorMap ta, tb;  // B in half boxes of 128 rows: one per CTA of a pair
-        if (!make_tmap(&ta, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM) ||
-            !make_tmap(&tb, B_t, static_cast<uint64_t>(K), static_cast<uint64_t>(N), 128))
-            return cudaErrorInvalidValue;
-        return launch_nt<256, true>(ta, tb, M, N, static_cast<int>(K), eps, pp.s, C, nullptr,
-                                    nullptr, device, kWaitLimitNs, stream);
-    }
     const RSched s = rng_sched(M, K, N, num_sms);
     const int NT = tile_cols(N);
     CUtensorMap ta, tb;
@@ -1039,10 +784,10 @@ cudaError_t launch_rmsnorm_gemm(const uint16_t *A, const uint16_t *B_t, int64_t 
     }
     const int Ki = static_cast<int>(K);
     switch (NT) {
-    case 32: return launch_nt<32, false>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
-    case 64: return launch_nt<64, false>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
-    case 128: return launch_nt<128, false>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
-    default: return launch_nt<256, false>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    case 32: return launch_nt<32>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    case 64: return launch_nt<64>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    case 128: return launch_nt<128>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
+    default: return launch_nt<256>(ta, tb, M, N, Ki, eps, s, C, tickets, partials, device, kWaitLimitNs, stream);
     }
 }
 

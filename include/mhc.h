@@ -47,6 +47,10 @@
  *   - B < 2^31; 1 <= n <= 8; C >= 8, C % 8 == 0 and n*C <= 2^30;
  *     otherwise MHC_ERR_UNSUPPORTED;
  *   - pointers non-NULL (MHC_ERR_INVALID) and 16-byte aligned (MHC_ERR_ALIGN);
+ *   - every device pointer (every pointer but mhc_forward_host's host
+ *     activations) is device memory of the current device, as
+ *     cudaPointerGetAttributes reports it: host memory, managed memory or
+ *     another GPU's memory reached over peer access is MHC_ERR_INVALID;
  *   - an output may not overlap any input or another output
  *     (MHC_ERR_INVALID), except that X_next may be exactly X;
  *   - iters >= 0 (MHC_ERR_INVALID);
@@ -325,9 +329,10 @@ int mhc_rmsnorm_gemm(const mhc_bf16 *A, const mhc_bf16 *B_t, int64_t M, int64_t 
  * - Same argument rules and status codes as mhc_gemm_rms.  A problem that
  *   needs more than MHC_NOALLOC_SCRATCH_BYTES of scratch is rejected with
  *   MHC_ERR_WORKSPACE before anything is launched.
- * - The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any
- *   stream capture on that device.
+ * - Every call looks up the array's device address in the current context
+ *   (the lookup allocates nothing), so a context created anew is served too.
+ *   The first call on a device loads the library's device code there: make it
+ *   before any stream capture on that device.
  * - Every call on a device shares the one array and it keeps the last call's
  *   contents (each call clears what must start at zero itself).  Calls that
  *   overlap on the GPU — on different streams, or from different threads

@@ -111,6 +111,14 @@ int mhc_testing_recip(const float *in, float *out, int64_t count, mhc_stream_t s
  */
 int mhc_testing_host_chunks(int64_t B, int64_t *sizes, int64_t capacity, int64_t *count);
 
+/*
+ * Turns the device-memory pointer checks of the device entry points off
+ * (on = 0) or on (on != 0), process-wide, and returns the previous setting.
+ * They are on unless this is called; switching them off only serves to time
+ * what they cost on the host.  The other argument checks always run.
+ */
+int mhc_testing_memory_checks(int on);
+
 #ifdef __cplusplus
 }
 #endif
