@@ -14,10 +14,11 @@ Reported:
                overlaps them chunk by chunk; the weights stay on the device)
   roofline     the dominant kernel's algorithmic bytes / its CUDA-event time,
                against the measured HBM copy bandwidth (MEASURED_PEAKS.json)
-  cpu_baseline the fp64 oracle on the host cores, on a bounded token sample
+  cpu_baseline the fp64 oracle split by token range over every host core, with its
+               one-core rate beside it, on a bounded token sample
   clocks       nvidia-smi samples taken while the timed steps run
 
-``--impl reference`` times the fp64 oracle instead (host cores only).
+``--impl reference`` times the fp64 oracle instead (every host core, no GPU).
 Under torchrun (N > 1) each rank drives its own GPU; rank 0 prints.
 """
 from __future__ import annotations
@@ -180,8 +181,8 @@ class ClockSampler:
 
 
 def cpu_oracle_rate(wl, inp, budget_s: float, chunk: int = 128):
-    """Tokens/s of the fp64 oracle forward on the first tokens of the workload,
-    in chunks of `chunk` tokens until `budget_s` seconds of oracle time."""
+    """Tokens/s of the fp64 oracle forward on one core: the first tokens of the
+    workload, in chunks of `chunk` tokens until `budget_s` seconds of oracle time."""
     import oracle
 
     phi = np.ascontiguousarray(inp["phi_t"].T)
@@ -196,6 +197,43 @@ def cpu_oracle_rate(wl, inp, budget_s: float, chunk: int = 128):
         elapsed += time.perf_counter() - t
         done += rows
     return done / elapsed, done, elapsed
+
+
+class OracleOnAllCores:
+    """The same single-threaded fp64 oracle forward, split by token range over a
+    pool of host threads (tokens are independent; the oracle's C call releases
+    the GIL).  Outputs land in per-range buffers and are discarded."""
+
+    def __init__(self, wl, inp, workers: int = 0, chunk: int = 32):
+        import concurrent.futures
+
+        import oracle
+
+        self.oracle = oracle
+        self.wl, self.inp, self.chunk = wl, inp, chunk
+        self.phi = np.ascontiguousarray(inp["phi_t"].T)
+        self.workers = workers or os.cpu_count() or 1
+        self.pool = concurrent.futures.ThreadPoolExecutor(self.workers)
+
+    def _part(self, lo, hi):
+        wl, inp = self.wl, self.inp
+        self.oracle.forward(inp["X"][lo:hi], self.phi, inp["F_out"][lo:hi], wl.n, wl.C,
+                            wl.alpha_pre, wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters)
+
+    def run(self, lo: int, hi: int) -> None:
+        futs = [self.pool.submit(self._part, a, min(a + self.chunk, hi))
+                for a in range(lo, hi, self.chunk)]
+        for f in futs:
+            f.result()
+
+    def rate(self, tokens: int):
+        """Tokens/s over the first `tokens` tokens (wall clock, all workers)."""
+        t = time.perf_counter()
+        self.run(0, tokens)
+        return tokens / (time.perf_counter() - t), time.perf_counter() - t
+
+    def close(self):
+        self.pool.shutdown()
 
 
 def cpu_model() -> str:
@@ -213,27 +251,25 @@ def run_reference(args, wl):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    # each step: the oracle forward over a bounded sample of the workload's tokens
-    tokens_per_step = args.ref_tokens
-    import oracle
+    # each step: the oracle forward over a bounded sample of the workload's tokens,
+    # split by token range over every host core
+    cores = os.cpu_count() or 1
+    tokens_per_step = args.ref_tokens or 32 * cores
     import synth
 
     inp = synth.make_inputs(wl, 0, rows=tokens_per_step)
-    phi = np.ascontiguousarray(inp["phi_t"].T)
-
-    def step():
-        oracle.forward(inp["X"], phi, inp["F_out"], wl.n, wl.C, wl.alpha_pre, wl.alpha_post,
-                       wl.alpha_res, inp["bias"], wl.iters)
+    pool = OracleOnAllCores(wl, inp, cores)
 
     for _ in range(args.warmup):
-        step()
+        pool.run(0, tokens_per_step)
     t = time.perf_counter()
     for _ in range(args.steps):
-        step()
+        pool.run(0, tokens_per_step)
     el = time.perf_counter() - t
+    pool.close()
     value = tokens_per_step * args.steps / el
-    sample = "first %d tokens of %s per step (fp64 oracle, 1 thread)" % (tokens_per_step,
-                                                                         wl.name)
+    sample = ("first %d tokens of %s per step (fp64 oracle, split by token range over %d "
+              "host threads)" % (tokens_per_step, wl.name, cores))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
@@ -241,7 +277,7 @@ def run_reference(args, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded counter-based generator)",
         "config": workload_config(wl, 1),
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
@@ -434,8 +470,9 @@ def main() -> int:
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for cpu_baseline")
-    ap.add_argument("--ref-tokens", type=int, default=128,
-                    help="tokens per step of the --impl reference arm")
+    ap.add_argument("--ref-tokens", type=int, default=0,
+                    help="tokens per step of the --impl reference arm (default 32 per host "
+                         "core)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--clock-window", type=float, default=1.0,
                     help="seconds of identical load kept up for the clock samples")
@@ -653,10 +690,21 @@ def main() -> int:
     # ---- CPU baseline: the fp64 oracle on the host cores (rank 0 only)
     cpu = None
     if rank == 0 and world == 1:
-        rate, tokens, secs = cpu_oracle_rate(wl, inp, args.cpu_budget)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": "first %d tokens of B=%d n=%d C=%d, fp64 oracle forward, %.1f s" % (
-                   tokens, B, n, C, secs), "cpu": cpu_model(), "host_cores": os.cpu_count()}
+        rate1, tokens1, secs1 = cpu_oracle_rate(wl, inp, args.cpu_budget)
+        cores = os.cpu_count() or 1
+        pool = OracleOnAllCores(wl, inp, cores)
+        # all cores: as many tokens as the 1-core leg's budget covers on every core
+        tok_all = min(B, max(cores * 32, int(rate1 * args.cpu_budget * cores / 2)))
+        rate_all, secs_all = pool.rate(tok_all)
+        pool.close()
+        cpu = {"value": rate_all, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": "first %d tokens of B=%d n=%d C=%d, fp64 oracle forward split by "
+                         "token range over %d host threads, %.1f s" % (
+                             tok_all, B, n, C, cores, secs_all),
+               "cpu": cpu_model(), "host_cores": os.cpu_count(),
+               "single_core": {"value": rate1, "unit": "tokens/s", "cores": 1,
+                               "sample": "first %d tokens, one thread, %.1f s" % (tokens1,
+                                                                                  secs1)}}
 
     if dist is not None:
         dist.barrier()

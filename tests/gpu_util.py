@@ -8,6 +8,9 @@ Tolerances (stated for the mHC forward this library implements):
   products): |ΔY| <= 1e-5·Σ_q|X[b,q]·φ[q,k]| + 1e-6, far above the typical
   sqrt(K)·2^-24 rounding and far below the effect of a dropped 64-wide K block.
 """
+import concurrent.futures
+import os
+
 import numpy as np
 import torch
 
@@ -95,3 +98,24 @@ def sample_rows(B: int, k: int = 48, seed: int = 0) -> np.ndarray:
     extra = rng.choice(B, size=min(k, B), replace=False)
     rows = sorted(r for r in fixed.union(extra.tolist()) if 0 <= r < B)
     return np.array(rows, dtype=np.int64)
+
+
+def for_all_rows(B: int, fn, chunk: int = 256, workers: int = 0) -> None:
+    """Run ``fn(lo, hi)`` over every token range [lo, hi) of [0, B) on all host
+    cores and re-raise the first failure.  Tokens are independent, so the
+    single-threaded oracle can take a range at a time; its C call and numpy's
+    array operations release the GIL."""
+    workers = workers or os.cpu_count() or 4
+    with concurrent.futures.ThreadPoolExecutor(workers) as ex:
+        futs = [ex.submit(fn, lo, min(lo + chunk, B)) for lo in range(0, B, chunk)]
+        for f in futs:
+            f.result()
+
+
+def host_outputs(out: dict) -> dict:
+    """A forward's outputs on the host: fp32 ones widened to float64, bf16 ones
+    kept as bit patterns (half the bytes of a float64 copy at full size)."""
+    g = {k: host64(out[k]) for k in ("Y", "r", "H_pre", "H_post", "H_res")}
+    for k in ("F_pre", "X_next"):
+        g[k] = host_bits(out[k])
+    return g

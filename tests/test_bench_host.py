@@ -90,7 +90,8 @@ def test_reference_arm_on_cpu():
     assert res.returncode == 0, res.stderr
     line = json.loads(res.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["unit"] == "tokens/s" and line["value"] > 0
-    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] == 1
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == (os.cpu_count() or 1)  # split over every host core
     assert line["e2e"]["h2d_bytes_per_step"] == 0
 
 
@@ -100,3 +101,29 @@ def test_reference_arm_other_ranks_are_silent():
                           "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
                          env=env, timeout=120)
     assert res.returncode == 0 and res.stdout.strip() == ""
+
+
+def test_oracle_on_all_cores_covers_every_token_once():
+    """The all-core CPU baseline runs the same oracle over disjoint token ranges: its
+    outputs, gathered, equal one single-threaded call over the whole range."""
+    import numpy as np
+
+    import bench
+    import oracle
+    import synth
+
+    wl = synth.WORKLOADS["tiny"].with_(B=70)
+    inp = synth.make_inputs(wl, 0)
+    pool = bench.OracleOnAllCores(wl, inp, workers=3, chunk=16)
+    got = {}
+    pool._part = lambda lo, hi: got.__setitem__((lo, hi), oracle.forward(
+        inp["X"][lo:hi], pool.phi, inp["F_out"][lo:hi], wl.n, wl.C, wl.alpha_pre,
+        wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters))
+    pool.run(0, wl.B)
+    pool.close()
+    assert sorted(got) == [(a, min(a + 16, 70)) for a in range(0, 70, 16)]
+    whole = oracle.forward(inp["X"], pool.phi, inp["F_out"], wl.n, wl.C, wl.alpha_pre,
+                           wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters)
+    for k in ("Y", "H_res", "X_next"):
+        parts = np.concatenate([got[key][k] for key in sorted(got)])
+        assert np.array_equal(parts, whole[k])

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import H_TOL, R_REL, assert_abs, assert_rel, cuda_ok, host64, sample_rows
+from gpu_util import H_TOL, R_REL, assert_abs, assert_rel, cuda_ok, for_all_rows, host64
 from synth import WORKLOADS
 
 pytestmark = [pytest.mark.gpu,
@@ -130,8 +130,9 @@ def test_forward_e4m3_matches_oracle(B, n, C):
     assert_e4m3_close(host8(X_next), ref["X_next"], "X_next", xn)
 
 
-def test_forward_e4m3_prefill_shape_sampled():
-    """B=16384, n=4, C=7168 in e4m3 (470 MB of X), rows sampled for the oracle."""
+def test_forward_e4m3_prefill_every_token():
+    """B=16384, n=4, C=7168 in e4m3 (470 MB of X): every token against the oracle, a
+    token range per host core."""
     wl = WORKLOADS["prefill"]
     B, n, C = wl.B, wl.n, wl.C
     X, P, Fo, bias = inputs(B, n, C, seed=83)
@@ -142,11 +143,22 @@ def test_forward_e4m3_prefill_shape_sampled():
                          torch.from_numpy(bias).cuda(), wl.iters, B, n, C, out["Y"], out["r"],
                          out["H_pre"], out["H_post"], out["H_res"], F_pre, X_next, out["ws"])
     torch.cuda.synchronize()
-    rows = sample_rows(B, 24)
-    ref = oracle.forward_e4m3(X[rows], np.ascontiguousarray(P.T), Fo[rows], n, C, wl.alpha_pre,
-                              wl.alpha_post, wl.alpha_res, bias, wl.iters)
-    for k in ("H_pre", "H_post", "H_res"):
-        assert_abs(host64(out[k])[rows], ref[k], H_TOL, k)
-    fp, xn = mix_absdots(X[rows], Fo[rows], ref, n, C)
-    assert_e4m3_close(host8(F_pre)[rows], ref["F_pre"], "F_pre", fp)
-    assert_e4m3_close(host8(X_next)[rows], ref["X_next"], "X_next", xn)
+    g = {k: host64(out[k]) for k in ("Y", "r", "H_pre", "H_post", "H_res")}
+    g_fp, g_xn = host8(F_pre), host8(X_next)
+    PT = np.ascontiguousarray(P.T)
+    absP = np.abs(dec(P)).T
+
+    def part(lo, hi):
+        ref = oracle.forward_e4m3(X[lo:hi], PT, Fo[lo:hi], n, C, wl.alpha_pre, wl.alpha_post,
+                                  wl.alpha_res, bias, wl.iters)
+        what = " (tokens %d-%d)" % (lo, hi - 1)
+        Yb = 1e-5 * (np.abs(dec(X[lo:hi])) @ absP) + 1e-6
+        assert np.all(np.abs(g["Y"][lo:hi] - ref["Y"]) <= Yb), "Y" + what
+        assert_rel(g["r"][lo:hi], ref["r"], R_REL, "r" + what)
+        for k in ("H_pre", "H_post", "H_res"):
+            assert_abs(g[k][lo:hi], ref[k], H_TOL, k + what)
+        fp, xn = mix_absdots(X[lo:hi], Fo[lo:hi], ref, n, C)
+        assert_e4m3_close(g_fp[lo:hi], ref["F_pre"], "F_pre" + what, fp)
+        assert_e4m3_close(g_xn[lo:hi], ref["X_next"], "X_next" + what, xn)
+
+    for_all_rows(B, part)

@@ -9,7 +9,8 @@ import torch
 import oracle
 import synth
 from gpu_util import (H_TOL, R_REL, assert_abs, assert_bf16_close, assert_rel, assert_Y_close,
-                      cuda_ok, dev_bf16, dev_f32, f64, host64, host_bits, phi_KN, sample_rows)
+                      cuda_ok, dev_bf16, dev_f32, f64, for_all_rows, host64, host_bits,
+                      host_outputs, phi_KN)
 from synth import WORKLOADS, make_inputs
 
 pytestmark = [pytest.mark.gpu,
@@ -258,25 +259,46 @@ def test_forward_full_oracle(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl, seed=0)
     out = forward_gpu(inp, wl)
-    check_forward(out, inp, wl)
+    check_forward_all_rows(out, inp, wl)
     check_properties(out, wl)
+
+
+def check_forward_all_rows(out, inp, wl):
+    """Every token of a large workload against the oracle, a token range per host core."""
+    g = host_outputs(out)
+    phi = phi_KN(inp["phi_t"])
+
+    def part(lo, hi):
+        ref = oracle.forward(inp["X"][lo:hi], phi, inp["F_out"][lo:hi], wl.n, wl.C,
+                             wl.alpha_pre, wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters)
+        what = " (tokens %d-%d)" % (lo, hi - 1)
+        assert_Y_close(g["Y"][lo:hi], ref["Y"], inp["X"][lo:hi], inp["phi_t"], "Y" + what)
+        assert_rel(g["r"][lo:hi], ref["r"], R_REL, "r" + what)
+        for k in ("H_pre", "H_post", "H_res"):
+            assert_abs(g[k][lo:hi], ref[k], H_TOL, k + what)
+        assert_bf16_close(f64(g["F_pre"][lo:hi]), ref["F_pre"], "F_pre" + what)
+        assert_bf16_close(f64(g["X_next"][lo:hi]), ref["X_next"], "X_next" + what)
+
+    for_all_rows(wl.B, part)
 
 
 @pytest.mark.parametrize("name", ["wider_it5", "wider", "wider_it50"])
-def test_forward_wider_sampled(name):
+def test_forward_wider_every_token(name):
+    """B=8192, n=8, C=4096, Student-t X: every token and every element."""
     wl = WORKLOADS[name]
     inp = make_inputs(wl, seed=0)
     out = forward_gpu(inp, wl)
-    check_forward(out, inp, wl, rows=sample_rows(wl.B, 40))
+    check_forward_all_rows(out, inp, wl)
     check_properties(out, wl)
 
 
-def test_forward_prefill_full_size_sampled():
-    """B=16384, n=4, C=7168 in the launch configuration the benchmark times."""
+def test_forward_prefill_every_token():
+    """B=16384, n=4, C=7168 in the launch configuration the benchmark times: every token
+    and every element against the oracle."""
     wl = WORKLOADS["prefill"]
     inp = make_inputs(wl, seed=0)
     out = forward_gpu(inp, wl)
-    check_forward(out, inp, wl, rows=sample_rows(wl.B, 48))
+    check_forward_all_rows(out, inp, wl)
     check_properties(out, wl)
     # run again: bitwise identical (fixed split-K order)
     Y0, X0 = out["Y"].clone(), out["X_next"].clone()

@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 from gpu_util import (H_TOL, R_REL, assert_abs, assert_bf16_close, assert_rel, cuda_ok,
-                      dev_bf16, dev_f32, f64, host64, host_bits, sample_rows)
+                      dev_bf16, dev_f32, f64, for_all_rows, host64, host_bits, host_outputs)
 from synth import WORKLOADS, make_inputs
 
 pytestmark = [pytest.mark.gpu,
@@ -88,7 +88,8 @@ def test_post_res_apply_f32_matches_oracle(inplace):
     assert_bf16_close(host64(out), ref, "X_next")
 
 
-def forward_f32w(wl, seed, rows=None):
+def forward_f32w(wl, seed):
+    """The fp32-weight forward on every token, against the oracle a token range per host core."""
     inp = make_inputs(wl, seed=seed, parts=("X", "bias"))
     X = inp["X"]
     phi = phi_f32(wl.n, wl.C, seed)
@@ -99,18 +100,22 @@ def forward_f32w(wl, seed, rows=None):
                          out["r"], out["H_pre"], out["H_post"], out["H_res"], out["F_pre"],
                          out["X_next"], out["ws"])
     torch.cuda.synchronize()
-    sel = np.arange(wl.B) if rows is None else np.asarray(rows)
-    ref = oracle.forward_f64w(X[sel], np.ascontiguousarray(phi.T).astype(np.float64),
-                              Fo[sel].astype(np.float64), wl.n, wl.C, wl.alpha_pre,
-                              wl.alpha_post, wl.alpha_res, inp["bias"], wl.iters)
-    g = {k: host64(out[k])[sel] for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre",
-                                          "X_next")}
-    assert_Y_f32(g["Y"], ref["Y"], X[sel], phi)
-    assert_rel(g["r"], ref["r"], R_REL, "r")
-    for k in ("H_pre", "H_post", "H_res"):
-        assert_abs(g[k], ref[k], H_TOL, k)
-    assert_bf16_close(g["F_pre"], ref["F_pre"], "F_pre")
-    assert_bf16_close(g["X_next"], ref["X_next"], "X_next")
+    g = host_outputs(out)
+    phi_kn = np.ascontiguousarray(phi.T).astype(np.float64)
+
+    def part(lo, hi):
+        ref = oracle.forward_f64w(X[lo:hi], phi_kn, Fo[lo:hi].astype(np.float64), wl.n, wl.C,
+                                  wl.alpha_pre, wl.alpha_post, wl.alpha_res, inp["bias"],
+                                  wl.iters)
+        what = " (tokens %d-%d)" % (lo, hi - 1)
+        assert_Y_f32(g["Y"][lo:hi], ref["Y"], X[lo:hi], phi)
+        assert_rel(g["r"][lo:hi], ref["r"], R_REL, "r" + what)
+        for k in ("H_pre", "H_post", "H_res"):
+            assert_abs(g[k][lo:hi], ref[k], H_TOL, k + what)
+        assert_bf16_close(f64(g["F_pre"][lo:hi]), ref["F_pre"], "F_pre" + what)
+        assert_bf16_close(f64(g["X_next"][lo:hi]), ref["X_next"], "X_next" + what)
+
+    for_all_rows(wl.B, part)
 
 
 @pytest.mark.parametrize("name", ["tiny", "decode1", "decode128"])
@@ -118,9 +123,8 @@ def test_forward_f32w_matches_oracle(name):
     forward_f32w(WORKLOADS[name], seed=74)
 
 
-def test_forward_f32w_7b_sampled():
-    wl = WORKLOADS["7b"]
-    forward_f32w(wl, seed=75, rows=sample_rows(wl.B, 40))
+def test_forward_f32w_7b_every_token():
+    forward_f32w(WORKLOADS["7b"], seed=75)
 
 
 def test_forward_f32w_wider_n8():
@@ -132,7 +136,7 @@ def test_forward_f32w_chain_every_n(n):
     """Above 3072 tokens the forward takes the kernel chain, whose split-weight GEMM forms
     the coefficients in its finalize: one GEMM width per n (2N padded to 16)."""
     wl = WORKLOADS["tiny"].with_(B=3200, n=n, C=64, bias_std=0.3)
-    forward_f32w(wl, seed=77 + n, rows=sample_rows(wl.B, 64))
+    forward_f32w(wl, seed=77 + n)
 
 
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 6, 7])
