@@ -333,8 +333,11 @@ def test_gemm_rms_coeffs_equals_the_two_calls(B, n, C, iters):
 
 
 # shapes for the one-kernel steps 1-4a path (test hook): a ragged last tile, a
-# ragged last chunk of tiles, n=8, a single chunk, and the 7B-width workload
-FUSED_SHAPES = [(1000, 4, 7168), (1100, 4, 4096), (600, 8, 2048), (256, 4, 2048), (4096, 4, 4096)]
+# ragged last chunk of tiles, every n from 1 to 8, a single chunk, and the
+# 7B-width workload
+FUSED_SHAPES = [(1000, 4, 7168), (1100, 4, 4096), (600, 8, 2048), (256, 4, 2048), (4096, 4, 4096),
+                (300, 3, 2048), (257, 1, 8192), (2000, 4, 8192), (129, 3, 3072), (700, 6, 1024),
+                (520, 5, 512), (900, 7, 256), (3000, 2, 1000)]
 
 
 @pytest.mark.parametrize("B,n,C", FUSED_SHAPES)
@@ -349,12 +352,31 @@ def test_forward_fused_path_shapes(B, n, C):
         assert torch.equal(out[k], again[k]), k  # fixed-order sums: bitwise reproducible
 
 
-def test_forward_fused_path_rejects_one_tile():
-    wl = WORKLOADS["tiny"]
+@pytest.mark.parametrize("B,n,C", [(64, 4, 256), (1, 4, 7168), (128, 8, 1024)])
+def test_forward_fused_path_rejects_one_tile(B, n, C):
+    wl = WORKLOADS["tiny"].with_(B=B, n=n, C=C)
     inp = make_inputs(wl, seed=6)
     with pytest.raises(mhc.MhcError) as ei:
         forward_gpu(inp, wl, path="fused")
     assert ei.value.status == mhc.MHC_ERR_UNSUPPORTED
+
+
+def test_forward_fused_path_f_pre_uses_the_written_h_pre():
+    """The finisher forms H_pre of its rows for F_pre; the stored H_pre comes from the
+    coefficient warp.  With X one-hot over the streams (channel c only in stream
+    c mod n), F_pre[c] is the bf16 rounding of the fp32 product H_pre[c mod n]·x[c],
+    bit for bit, so a finisher that used other bits would show."""
+    B, n, C = 300, 4, 4096
+    wl = WORKLOADS["decode1"].with_(B=B, n=n, C=C, bias_std=0.3)
+    inp = make_inputs(wl, seed=9)
+    x = inp["X"].reshape(B, n, C)
+    keep = (np.arange(C)[None, :] % n) == np.arange(n)[:, None]
+    inp["X"] = np.where(keep[None], x, np.uint16(0)).reshape(B, n * C).astype(np.uint16)
+    out = forward_gpu(inp, wl, path="fused")
+    Hp = host64(out["H_pre"])
+    xs = f64(inp["X"]).reshape(B, n, C)[:, np.arange(C) % n, np.arange(C)]
+    prod32 = (Hp[:, np.arange(C) % n] * xs).astype(np.float32)
+    assert np.array_equal(host_bits(out["F_pre"]), synth.f32_to_bf16_bits(prod32))
 
 
 @pytest.mark.parametrize("B,n,C", ODD_SHAPES)
