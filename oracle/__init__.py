@@ -10,9 +10,12 @@ thread, index-order sums), a restatement of §2.1–§2.5 of the page
 "Towards Free Normalization: Fusing Normalization into GEMM and Attention
 Kernels" (``rmsnorm_gemm``).  This module only marshals numpy arrays.
 
-Pins: every function here is checked in ``tests/test_oracle_pins.py``
-against closed forms, invariants, one-hot special cases and exact-integer
-results (see the design notes for the list); no function is left unpinned.
+Pins: every function here is checked in ``tests/test_oracle_pins.py`` (the
+pins themselves are in ``tests/oracle_pins.py``) against hand-derived worked
+examples, closed forms, Sinkhorn invariants, one-hot special cases and
+exact-integer results; ``tests/test_oracle_mutants.py`` plants 26 one-line
+mistakes in a copy of the C source and checks that pins catch each.  No
+function is left unpinned.
 """
 from __future__ import annotations
 

@@ -8,8 +8,7 @@
  * cuTile implementation), §2.1–§2.5.  Sums run in index order in double
  * precision.  See mhc_oracle.h for shapes and layouts.
  *
- * Readings taken where the page is silent or garbled (each is listed in the
- * design notes):
+ * Readings taken where the page is silent or garbled:
  *   - r has no epsilon (§2.2 and the r computation of §4.1 add none);
  *   - sigmoid(x) = 1 / (1 + exp(-x)) (§2.4; the helper's body is not shown);
  *   - Sinkhorn starts from exp(H̃_res) and each iteration normalises the rows,
