@@ -486,7 +486,7 @@ def main() -> int:
                          "pairs, fp32 F_out), e4m3 times mhc_forward_e4m3 (fp8 activations "
                          "and weight), instead of the bf16 forward")
     ap.add_argument("--tokens", type=int, default=None,
-                    help="latency mode: the workload with this many tokens instead")
+                    help="latency and kernels modes: the workload with this many tokens instead")
     ap.add_argument("--mode", default="full",
                     choices=["full", "kernels", "latency", "rmsnorm_gemm"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
@@ -502,8 +502,8 @@ def main() -> int:
 
     wl = synth.WORKLOADS[args.workload]
     if args.tokens is not None:
-        if args.mode != "latency":
-            ap.error("--tokens only applies to --mode latency")
+        if args.mode not in ("latency", "kernels"):
+            ap.error("--tokens only applies to --mode latency and --mode kernels")
         wl = wl.with_(name="%s_B%d" % (wl.name, args.tokens), B=args.tokens)
     if args.impl == "reference":
         return run_reference(args, wl)

@@ -47,6 +47,8 @@ constexpr int kEpiThreads = 128;
 constexpr int kReduceItems = 16;  // outputs per thread per round of the fixed-order sum
 constexpr int kReduceBatch = 4;   // contributors loaded per batch: 64 loads in flight
 constexpr int kRingBudget = 200 * 1024;
+// columns of a row that the final segment's shared-memory sum takes at once
+constexpr int kSumCols = 16;
 
 __device__ int g_device_status;
 
@@ -106,7 +108,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     pipe::Pipe p;
     pipe::carve<NPAD, kRingBudget>(p, smem, &g_device_status, wait_limit_ns);
-    uint64_t *epi_bar = p.extra;  // epilogue group barrier
+    uint64_t *epi_bar = p.extra;      // epilogue group barrier
+    uint64_t *red_bar = p.extra + 1;  // [2]: a chunk of the final segment's partials landed
     volatile int *is_last = p.abort + 1;
 
     const int warp = threadIdx.x >> 5;
@@ -116,6 +119,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     if (threadIdx.x == 0) {
         pipe::init_barriers(p);
         ptx::mbar_init(epi_bar, kEpiThreads);
+        ptx::mbar_init(red_bar, 1);
+        ptx::mbar_init(red_bar + 1, 1);
         *is_last = 0;
         ptx::fence_barrier_init();
     }
@@ -223,13 +228,129 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
             if (*is_last) {
                 __threadfence();
-                // fixed-order sum over the contributors first..last: a batch of
-                // contributors x items is loaded before it is added, in order
                 const int rows = static_cast<int>((B - row0) < kBM ? (B - row0) : kBM);
                 const int items = kBM * stride;  // item i: column i / kBM, row i % kBM
                 const float *p0 = partials + static_cast<int64_t>(first + sg.m) * kBM * stride;
                 const int64_t slot_stride = static_cast<int64_t>(kBM) * stride;
                 const int nc = last - first + 1;
+                SegIter peek = it;
+                Segment nx;
+                // This CTA's last segment: its stage ring is idle (every stage has been
+                // consumed).  The contributors' partials come into it by bulk copies, a
+                // chunk of columns of every contributor at a time, two chunks in
+                // flight; loads into registers would take one round trip per batch of
+                // contributors, and this sum ends the kernel on the critical path.
+                const int rs = stride | 1;  // odd row pitch: the row writes miss no bank
+                const uint32_t row_bytes = static_cast<uint32_t>(kBM) * rs * 4;
+                const int64_t room = (C::kRingBytes - static_cast<int64_t>(row_bytes)) / 2;
+                const int cc = static_cast<int>(
+                    min(static_cast<int64_t>(stride), room / (static_cast<int64_t>(nc) * kBM * 4)));
+                if (!peek.next(nx) && cc > 0) {
+                    float *rowbuf = reinterpret_cast<float *>(p.stages);  // [kBM][rs]
+                    float *const chunk0 = rowbuf + kBM * rs;  // two buffers, [nc][cc][kBM]
+                    const int64_t half = static_cast<int64_t>(nc) * cc * kBM;
+                    const int nchunks = (stride + cc - 1) / cc;
+                    auto issue = [&](int k) {
+                        const int c0 = k * cc;
+                        const int w = min(cc, stride - c0);
+                        const uint32_t bytes = static_cast<uint32_t>(w) * kBM * 4;
+                        ptx::mbar_arrive_expect_tx(red_bar + (k & 1), bytes * nc);
+                        for (int c = 0; c < nc; ++c)
+                            ptx::bulk_load(chunk0 + (k & 1) * half + static_cast<int64_t>(c) * cc * kBM,
+                                           p0 + c * slot_stride + static_cast<int64_t>(c0) * kBM,
+                                           bytes, red_bar + (k & 1), ptx::policy_evict_first());
+                    };
+                    if (et == 0) {
+                        // the partials were written through the generic proxy
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                        issue(0);
+                        if (nchunks > 1) issue(1);
+                    }
+                    bool ok = true;
+                    int k = 0;
+                    for (; k < nchunks; ++k) {
+                        if (!pipe::wait(p, red_bar + (k & 1), (k >> 1) & 1)) {
+                            ok = false;
+                            break;
+                        }
+                        // thread et: row et, its contributors in order as in the
+                        // general path below, so the sums agree to the bit
+                        if (et < rows) {
+                            const float *buf = chunk0 + (k & 1) * half + et;
+                            const int c0 = k * cc;
+                            const int w = min(cc, stride - c0);
+                            // kSumCols columns at once: their loads are independent
+                            for (int col0 = 0; col0 < w; col0 += kSumCols) {
+                                float acc[kSumCols];
+#pragma unroll
+                                for (int u = 0; u < kSumCols; ++u) acc[u] = 0.f;
+#pragma unroll 2
+                                for (int c = 0; c < nc; ++c) {
+                                    const float *src = buf + (static_cast<int64_t>(c) * cc + col0) * kBM;
+                                    float v[kSumCols];
+#pragma unroll
+                                    for (int u = 0; u < kSumCols; ++u)
+                                        v[u] = col0 + u < w ? src[u * kBM] : 0.f;
+#pragma unroll
+                                    for (int u = 0; u < kSumCols; ++u) acc[u] += v[u];
+                                }
+#pragma unroll
+                                for (int u = 0; u < kSumCols; ++u)
+                                    if (col0 + u < w) rowbuf[et * rs + c0 + col0 + u] = acc[u];
+                            }
+                        }
+                        // every read of this chunk's buffer is done before it refills
+                        if (!pipe::group_sync(p, epi_bar, epi_phase)) {
+                            ok = false;
+                            break;
+                        }
+                        if (et == 0 && k + 2 < nchunks) issue(k + 2);
+                    }
+                    if (!ok) {
+                        // the copies issued land before the CTA may exit
+                        volatile int never = 0;
+                        for (int j = k; j < nchunks && j < k + 2; ++j)
+                            ptx::mbar_wait_bounded(red_bar + (j & 1), (j >> 1) & 1, &never,
+                                                   p.limit_ns);
+                        break;
+                    }
+                    // The tile's rows of Y are contiguous (and 16-byte aligned: row0 is
+                    // a multiple of 128): 16-byte stores, each thread's (row, column)
+                    // stepped along without a division.  N >= 3, so one wrap suffices.
+                    {
+                        float *yt = Y + row0 * N;
+                        const int total = rows * N, quads = total >> 2;
+                        const int srow = 4 * kEpiThreads / N, scol = 4 * kEpiThreads % N;
+                        int yr = 4 * et / N, yc = 4 * et % N;
+                        for (int q4 = et; q4 < quads; q4 += kEpiThreads) {
+                            float f[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const bool wrap = yc + u >= N;
+                                f[u] = rowbuf[(yr + wrap) * rs + yc + u - (wrap ? N : 0)];
+                            }
+                            *reinterpret_cast<float4 *>(yt + 4 * q4) = make_float4(f[0], f[1], f[2], f[3]);
+                            yc += scol;
+                            yr += srow;
+                            if (yc >= N) {
+                                yc -= N;
+                                ++yr;
+                            }
+                        }
+                        for (int i = 4 * quads + et; i < total; i += kEpiThreads)
+                            yt[i] = rowbuf[(i / N) * rs + i % N];
+                    }
+                    if (et < rows) {
+                        const float *yr = rowbuf + et * rs;
+                        const float rr = sqrtf(yr[N] / static_cast<float>(K));
+                        r[row0 + et] = rr;
+                        if (cf.H_pre) row_coeffs<NPAD, kSplit>(cf, yr, rr, row0 + et);
+                    }
+                    if (et == 0) tile_tickets[sg.m] = 0;
+                    continue;
+                }
+                // fixed-order sum over the contributors first..last: a batch of
+                // contributors x items is loaded before it is added, in order
                 for (int i0 = et; i0 < items; i0 += kEpiThreads * kReduceItems) {
                     float acc_s[kReduceItems];
 #pragma unroll
