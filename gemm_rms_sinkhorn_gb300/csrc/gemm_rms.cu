@@ -91,6 +91,47 @@ __device__ __forceinline__ void row_coeffs(const CoefArgs &cf, const float *y, f
     row_coeffs_n<NPAD, kSplit, 8>(cf, y, rb, t);
 }
 
+// The same for a pair of adjacent lanes (lane parity = half), each taking
+// half of the token's rows; every lane of the warp calls it.
+template <int NPAD, bool kSplit, int nn>
+__device__ __forceinline__ void pair_coeffs_n(const CoefArgs &cf, const float *y, float rb,
+                                              int half, bool store, int64_t t)
+{
+    if constexpr (kWidthOf<NPAD, kSplit, nn>) {
+        if (cf.n == nn) {
+            if constexpr (nn == 1) {
+                if (store && half == 0) {
+                    float hp[1], hq[1], m[1][1];
+                    token_coeffs<1>(y, rb, cf.bias, cf.a_pre, cf.a_post, cf.a_res, cf.iters, hp,
+                                    hq, m);
+                    store_token_coeffs<1>(t, hp, hq, m, cf.H_pre, cf.H_post, cf.H_res);
+                }
+            } else {
+                token_coeffs_pair<nn>(y, rb, cf.bias, cf.a_pre, cf.a_post, cf.a_res, cf.iters,
+                                      half, store, t, cf.H_pre, cf.H_post, cf.H_res);
+            }
+        }
+    }
+}
+
+// Coefficients of rows [64·g, 64·g + 64) of a finished tile whose rows (Ỹ then
+// Σx², pitch rs floats) sit in shared memory, on the 128 threads gt of group
+// g: a token per pair of lanes.  A lane past the tile's last row works on row
+// 0 and stores nothing.
+template <int NPAD, bool kSplit>
+__device__ __forceinline__ void tile_coeffs_share(const CoefArgs &cf, const float *rowbuf, int rs,
+                                                  int N, int K, int64_t row0, int rows, int g,
+                                                  int gt)
+{
+    const int tk = g * 64 + (gt >> 1);
+    const bool live = tk < rows;
+    const float *yr = rowbuf + (live ? tk : 0) * rs;
+    const float rb = sqrtf(yr[N] / static_cast<float>(K));
+#define MHC_PAIR(k) pair_coeffs_n<NPAD, kSplit, k>(cf, yr, rb, gt & 1, live, row0 + tk);
+    MHC_PAIR(1) MHC_PAIR(2) MHC_PAIR(3) MHC_PAIR(4) MHC_PAIR(5) MHC_PAIR(6) MHC_PAIR(7) MHC_PAIR(8)
+#undef MHC_PAIR
+}
+
 // kSplit: the weight operand holds every column twice, as the bf16 value
 // nearest the fp32 weight and the bf16 value nearest the remainder (rows 2k,
 // 2k+1 of φᵀ), and the epilogue adds each pair: Ỹ[k] = acc[2k] + acc[2k+1].
@@ -109,8 +150,10 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
     pipe::Pipe p;
     pipe::carve<NPAD, kRingBudget>(p, smem, &g_device_status, wait_limit_ns);
     uint64_t *epi_bar = p.extra;      // epilogue group barrier
-    uint64_t *red_bar = p.extra + 1;  // [2]: a chunk of the final segment's partials landed
+    uint64_t *red_bar = p.extra + 1;   // [2]: a chunk of the final segment's partials landed
+    uint64_t *coef_bar = p.extra + 3;  // the final tile's rows are in shared memory
     volatile int *is_last = p.abort + 1;
+    volatile int *coef_tile = p.abort + 2;  // 1 + that tile, or 0: no coefficients to help with
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -121,7 +164,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         ptx::mbar_init(epi_bar, kEpiThreads);
         ptx::mbar_init(red_bar, 1);
         ptx::mbar_init(red_bar + 1, 1);
+        ptx::mbar_init(coef_bar, kEpiThreads);
         *is_last = 0;
+        *coef_tile = 0;
         ptx::fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
@@ -147,6 +192,19 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         if (lane == 0) pipe::mma_issuer<NPAD, SegIter, kFp8>(p, segs);
     } else if (warp < 6) {
         pipe::square_sum<NPAD, SegIter, kFp8>(p, segs, (warp - 2) * 32 + lane, lane);
+        // then the second half of the last tile's coefficients, when this CTA
+        // finishes a tile in its last segment (the epilogue takes the first)
+        // a warp helps only if all its lanes saw the tile (the pair shuffles)
+        if (cf.H_pre && __all_sync(0xffffffffu, pipe::wait(p, coef_bar, 0))) {
+            const int m1 = *coef_tile;
+            if (m1 > 0) {
+                const int64_t row0 = static_cast<int64_t>(m1 - 1) * kBM;
+                const int rows = static_cast<int>((B - row0) < kBM ? (B - row0) : kBM);
+                tile_coeffs_share<NPAD, kSplit>(cf, reinterpret_cast<const float *>(p.stages),
+                                                (N + 1) | 1, N, K, row0, rows, 1,
+                                                threadIdx.x - 64);
+            }
+        }
     } else {
         // ----------------------------------------------- epilogue (warps 6..9)
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -154,6 +212,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
         const int et = threadIdx.x - 192;  // 0..127 within the epilogue group
         uint32_t epi_phase = 0;
         int seg = 0;
+        bool coef_arrived = false;  // each epilogue thread arrives on coef_bar once
         SegIter it = segs;
         Segment sg;
         while (it.next(sg)) {
@@ -340,13 +399,15 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         for (int i = 4 * quads + et; i < total; i += kEpiThreads)
                             yt[i] = rowbuf[(i / N) * rs + i % N];
                     }
-                    if (et < rows) {
-                        const float *yr = rowbuf + et * rs;
-                        const float rr = sqrtf(yr[N] / static_cast<float>(K));
-                        r[row0 + et] = rr;
-                        if (cf.H_pre) row_coeffs<NPAD, kSplit>(cf, yr, rr, row0 + et);
-                    }
+                    if (et < rows) r[row0 + et] = sqrtf(rowbuf[et * rs + N] / static_cast<float>(K));
                     if (et == 0) tile_tickets[sg.m] = 0;
+                    if (cf.H_pre) {
+                        // the square-sum warps, idle now, take rows 64..127
+                        if (et == 0) *coef_tile = static_cast<int>(sg.m) + 1;
+                        ptx::mbar_arrive(coef_bar);
+                        coef_arrived = true;
+                        tile_coeffs_share<NPAD, kSplit>(cf, rowbuf, rs, N, K, row0, rows, 0, et);
+                    }
                     continue;
                 }
                 // fixed-order sum over the contributors first..last: a batch of
@@ -389,6 +450,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 if (et == 0) tile_tickets[sg.m] = 0;
             }
         }
+        if (!coef_arrived) ptx::mbar_arrive(coef_bar);  // nothing to help with
     }
 
     // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before

@@ -136,9 +136,11 @@ __device__ __forceinline__ void token_coeffs(const float *y, float rb, const flo
                 }
 #pragma unroll
                 for (int j = 0; j < n; ++j) {
+                    // products rounded on their own (never fused into the sum's
+                    // adds), so a column sum split across lanes gives these bits
                     float p[n];
 #pragma unroll
-                    for (int i = 0; i < n; ++i) p[i] = u[i] * m[i][j];
+                    for (int i = 0; i < n; ++i) p[i] = __fmul_rn(u[i], m[i][j]);
                     v[j] = recip_approx(tree_sum<n>(p));
                 }
             }
@@ -146,6 +148,122 @@ __device__ __forceinline__ void token_coeffs(const float *y, float rb, const flo
             for (int i = 0; i < n; ++i)
 #pragma unroll
                 for (int j = 0; j < n; ++j) m[i][j] = (u[i] * m[i][j]) * v[j];
+        }
+    }
+}
+
+// token_coeffs for one token on a pair of adjacent lanes (lane parity =
+// half): half 0 takes rows [0, n/2) of H_res and those entries of H_pre and
+// H_post, half 1 rows [n/2, n), and each stores its own (when `store`).  Row
+// steps are local.  A column sum is the two halves' partial tree sums added,
+// which is exactly how tree_sum<n> splits (tree_sum<n/2> + tree_sum<n - n/2>),
+// and every other value is the same expression on the same operands, so the
+// result equals token_coeffs' to the bit (the column products are rounded
+// on their own in both, so no add fuses one of them in one form and not the
+// other).  Every lane of the warp must call it
+// (the column sums cross lanes); a lane with nothing to store passes
+// store = false.  n >= 2.
+template <int n>
+__device__ __forceinline__ void token_coeffs_pair(const float *y, float rb, const float *bias,
+                                                  float a_pre, float a_post, float a_res,
+                                                  int iters, int half, bool store, int64_t t,
+                                                  float *H_pre, float *H_post, float *H_res)
+{
+    static_assert(n >= 2, "a pair needs a row for each half");
+    constexpr int h0 = n / 2, kR = n - n / 2;  // rows of half 0; rows of half 1
+    const int i0 = half ? h0 : 0;
+    const int cnt = half ? kR : h0;
+    const float inv_r = 1.0f / rb;
+    // the other half's partial of a column sum, added in tree_sum<n>'s order
+    const auto col_total = [&](const float (&p)[kR]) {
+        const float own = half ? tree_sum<kR>(p) : tree_sum<h0>(p);
+        const float other = __shfl_xor_sync(0xffffffffu, own, 1);
+        return half ? other + own : own + other;
+    };
+    float m[kR][n];
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        const int i = r < cnt ? i0 + r : i0;  // a spare row (half 0, odd n) repeats row i0
+#pragma unroll
+        for (int j = 0; j < n; ++j)
+            m[r][j] = a_res * y[2 * n + i * n + j] * inv_r + bias[2 * n + i * n + j];
+    }
+    if (iters > 0) {
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+            float mx = m[r][0];
+#pragma unroll
+            for (int j = 1; j < n; ++j) mx = fmaxf(mx, m[r][j]);
+#pragma unroll
+            for (int j = 0; j < n; ++j) m[r][j] = expf(m[r][j] - mx);
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < kR; ++r)
+#pragma unroll
+            for (int j = 0; j < n; ++j) m[r][j] = expf(m[r][j]);
+    }
+    if constexpr (n <= 4) {
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int r = 0; r < kR; ++r) {
+                const float inv = recip_approx(tree_sum<n>(m[r]));
+#pragma unroll
+                for (int j = 0; j < n; ++j) m[r][j] *= inv;
+            }
+#pragma unroll
+            for (int j = 0; j < n; ++j) {
+                float col[kR];
+#pragma unroll
+                for (int r = 0; r < kR; ++r) col[r] = m[r][j];
+                const float inv = recip_approx(col_total(col));
+#pragma unroll
+                for (int r = 0; r < kR; ++r) m[r][j] *= inv;
+            }
+        }
+    } else {
+        if (iters > 0) {
+            float u[kR], v[n];
+#pragma unroll
+            for (int j = 0; j < n; ++j) v[j] = 1.0f;
+            for (int it = 0; it < iters; ++it) {
+#pragma unroll
+                for (int r = 0; r < kR; ++r) {
+                    float p[n];
+#pragma unroll
+                    for (int j = 0; j < n; ++j) p[j] = m[r][j] * v[j];
+                    u[r] = recip_approx(tree_sum<n>(p));
+                }
+#pragma unroll
+                for (int j = 0; j < n; ++j) {
+                    float p[kR];
+#pragma unroll
+                    for (int r = 0; r < kR; ++r) p[r] = __fmul_rn(u[r], m[r][j]);
+                    v[j] = recip_approx(col_total(p));
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < kR; ++r)
+#pragma unroll
+                for (int j = 0; j < n; ++j) m[r][j] = (u[r] * m[r][j]) * v[j];
+        }
+    }
+    if (!store) return;
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+        if (r >= cnt) break;
+        const int i = i0 + r;
+        H_pre[t * n + i] = pre_coeff(y[i], inv_r, a_pre, bias[i]);
+        H_post[t * n + i] = 2.0f * sigmoid(a_post * y[n + i] * inv_r + bias[n + i]);
+        float *o = H_res + (t * n + i) * n;
+        if constexpr (n % 4 == 0) {
+#pragma unroll
+            for (int j = 0; j < n; j += 4)
+                *reinterpret_cast<float4 *>(o + j) =
+                    make_float4(m[r][j], m[r][j + 1], m[r][j + 2], m[r][j + 3]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < n; ++j) o[j] = m[r][j];
         }
     }
 }

@@ -270,6 +270,16 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// 4-byte asynchronous copy global -> shared (both 4-byte aligned); completes
+// at the issuing thread's next cp_async_wait_all.
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void *p)
 {
     uint4 v;

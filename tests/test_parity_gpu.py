@@ -187,6 +187,59 @@ def test_post_res_apply(B, n, C, inplace):
     assert_bf16_close(host64(out), ref, "X_next")
 
 
+# Wide n (5..8) runs one wave of resident blocks that walk the tokens: these
+# batches exceed a wave's token rows (at most 152 SMs x 4 blocks at these
+# widths), so every block mixes several tokens through its double buffer.
+WIDE_WALK_SHAPES = [(3000, 5, 264), (2500, 6, 40), (1900, 7, 8), (4100, 8, 72), (700, 8, 4096)]
+
+
+@pytest.mark.parametrize("B,n,C", WIDE_WALK_SHAPES)
+def test_pre_apply_wide_walk(B, n, C):
+    X = synth.normal_bf16((B, n * C), 14, 0)
+    Hp = np.abs(synth.normal_f32((B, n), 15, 9, 0.5)) % 1.0
+    F = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+    mhc.mhc_pre_apply(dev_bf16(X), dev_f32(Hp), B, n, C, F)
+    torch.cuda.synchronize()
+    assert_bf16_close(host64(F), oracle.pre_apply(X, Hp.astype(np.float64), n, C), "F_pre")
+
+
+@pytest.mark.parametrize("B,n,C", WIDE_WALK_SHAPES)
+@pytest.mark.parametrize("inplace", [False, True])
+def test_post_res_apply_wide_walk(B, n, C, inplace):
+    X = synth.normal_bf16((B, n * C), 25, 0)
+    Fo = synth.normal_bf16((B, C), 25, 1)
+    Hr = oracle.sinkhorn(synth.normal_f32((B, n, n), 26, 9, 1.0), 20).astype(np.float32)
+    Hq = 2.0 * (np.abs(synth.normal_f32((B, n), 27, 9, 0.5)) % 1.0)
+    out = post_gpu(X, Fo, Hr, Hq, n, C, inplace)
+    ref = oracle.post_res_apply(X, Fo, Hr.astype(np.float64), Hq.astype(np.float64), n, C)
+    assert_bf16_close(host64(out), ref, "X_next")
+
+
+def test_wide_apply_token_walk_is_exact():
+    """Every token its own one-hot H_pre and permutation H_res: a coefficient
+    taken from the wrong token or the wrong half of the double buffer moves
+    whole streams, which an exact comparison sees."""
+    B, n, C = 3001, 8, 64
+    X = synth.normal_bf16((B, n * C), 28, 0)
+    Fo = synth.normal_bf16((B, C), 28, 1)
+    rng = np.random.default_rng(29)
+    sel = rng.integers(0, n, size=B)
+    Hp = np.zeros((B, n), dtype=np.float32)
+    Hp[np.arange(B), sel] = 1.0
+    F = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+    mhc.mhc_pre_apply(dev_bf16(X), dev_f32(Hp), B, n, C, F)
+    torch.cuda.synchronize()
+    Xr = X.reshape(B, n, C)
+    assert np.array_equal(host_bits(F), Xr[np.arange(B), sel, :])
+    perms = np.stack([rng.permutation(n) for _ in range(B)])
+    Hr = np.zeros((B, n, n), dtype=np.float32)
+    for i in range(n):
+        Hr[np.arange(B), i, perms[:, i]] = 1.0
+    out = post_gpu(X, Fo, Hr, np.zeros((B, n), dtype=np.float32), n, C)
+    want = np.take_along_axis(Xr, perms[:, :, None], axis=1)
+    assert np.array_equal(host_bits(out).reshape(B, n, C), want)
+
+
 def test_post_res_apply_permutation_is_exact():
     B, n, C = 5, 3, 64
     X = synth.normal_bf16((B, n * C), 24, 0)
