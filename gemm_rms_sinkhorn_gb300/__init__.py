@@ -18,11 +18,14 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libmhc_gb300.so")
+# MHC_GB300_CHECK=1 loads the build with device index checks (-DMHC_CHECK,
+# `python gemm_rms_sinkhorn_gb300/build.py --check`) instead of the default one.
+CHECK_BUILD = os.environ.get("MHC_GB300_CHECK", "0") not in ("", "0")
+LIB_PATH = os.path.join(_PKG, "libmhc_gb300_check.so" if CHECK_BUILD else "libmhc_gb300.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError("%s is missing: build it with `python gemm_rms_sinkhorn_gb300/build.py` "
-                      "(or __graft_entry__.build())" % LIB_PATH)
+    raise ImportError("%s is missing: build it with `python gemm_rms_sinkhorn_gb300/build.py%s` "
+                      "(or __graft_entry__.build())" % (LIB_PATH, " --check" if CHECK_BUILD else ""))
 
 _lib = ctypes.CDLL(LIB_PATH)
 
@@ -33,6 +36,7 @@ MHC_ERR_ALIGN = -3
 MHC_ERR_CUDA = -4
 MHC_ERR_TIMEOUT = -5
 MHC_ERR_WORKSPACE = -6
+MHC_ERR_BOUNDS = -7
 
 MHC_NOALLOC_SCRATCH_BYTES = 16 << 20  # include/mhc.h: the built-in scratch of mhc_gemm_rms_noalloc
 
@@ -82,6 +86,10 @@ _SIGS = {
     "mhc_testing_recip": ([_vp, _vp, _i64, _vp], _i32),
     "mhc_testing_host_chunks": ([_i64, _vp, _i64, ctypes.POINTER(_i64)], _i32),
     "mhc_testing_memory_checks": ([_i32], _i32),
+    "mhc_testing_check_build": ([], _i32),
+    "mhc_testing_check_record": ([ctypes.POINTER(_i32), ctypes.POINTER(_i64),
+                                  ctypes.POINTER(_i64)], _i32),
+    "mhc_testing_check_selftest": ([], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -420,6 +428,15 @@ def mhc_device_status() -> int:
     st = _i32(0)
     _check(_lib.mhc_device_status(ctypes.byref(st)), "mhc_device_status")
     return st.value
+
+
+def mhc_testing_check_record() -> tuple:
+    """(site, offset, extent) of the first failed device index check since the
+    last read (site 0: none), read and cleared; always (0, 0, 0) in the default build."""
+    site, off, ext = _i32(0), _i64(0), _i64(0)
+    _check(_lib.mhc_testing_check_record(ctypes.byref(site), ctypes.byref(off), ctypes.byref(ext)),
+           "mhc_testing_check_record")
+    return site.value, off.value, ext.value
 
 
 def alloc_outputs(B: int, n: int, C: int, device=None) -> dict:

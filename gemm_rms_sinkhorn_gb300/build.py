@@ -3,7 +3,8 @@
 Each ``csrc/*.cu`` file is compiled by its own ``nvcc`` process (in parallel)
 with ``-gencode arch=compute_103a,code=sm_103a``, then the objects are linked
 into one shared library next to this file.  Only sources newer than their
-object are recompiled.  Run ``python gemm_rms_sinkhorn_gb300/build.py``.
+object are recompiled.  Run ``python gemm_rms_sinkhorn_gb300/build.py``
+(``--check``: the MHC_CHECK build, ``libmhc_gb300_check.so``, beside it).
 """
 from __future__ import annotations
 
@@ -20,6 +21,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmhc_gb300.so")
+# the build with device index checks (-DMHC_CHECK): same sources, own objects
+BUILD_CHECK = os.path.join(PKG, "_build_check")
+LIB_CHECK = os.path.join(PKG, "libmhc_gb300_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + INCLUDE,
@@ -48,16 +52,23 @@ def _compile(nvcc, src, obj, extra, verbose):
     return res.stdout + res.stderr
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          check: bool = False) -> str:
+    """Builds libmhc_gb300.so, or with check=True libmhc_gb300_check.so, whose
+    kernels record a failed device index check instead of touching memory out
+    of range (csrc/check.cuh)."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir, lib = (BUILD_CHECK, LIB_CHECK) if check else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest_hdr = max((os.path.getmtime(h) for h in _headers()), default=0.0)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if check:
+        extra.append("-DMHC_CHECK")
     jobs = []
     objs = []
     for src in srcs:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         stale = (force or ptxas_info or not os.path.exists(obj) or
                  os.path.getmtime(obj) < max(os.path.getmtime(src), newest_hdr))
@@ -69,15 +80,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         if ptxas_info:
             for (src, _), out in zip(jobs, outs):
                 print("== %s\n%s" % (os.path.basename(src), out))
-    if jobs or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(map(os.path.getmtime, objs)):
-        tmp = LIB + ".%d.tmp" % os.getpid()
+    if jobs or not os.path.exists(lib) or os.path.getmtime(lib) < max(map(os.path.getmtime, objs)):
+        tmp = lib + ".%d.tmp" % os.getpid()
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         if verbose:
             print(" ".join(cmd), flush=True)
         subprocess.check_call(cmd)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                check="--check" in sys.argv))

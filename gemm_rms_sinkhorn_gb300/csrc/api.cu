@@ -8,11 +8,55 @@
 #include <cstdint>
 #include <mutex>
 
+#include "check.cuh"
 #include "mhc.h"
 #include "mhc_internal.h"
 #include "mhc_testing.h"
 
 namespace mhc {
+
+// Readers of the per-file device check records (empty in the default build).
+namespace {
+std::mutex g_check_mu;
+CheckReader g_check_readers[16];
+int g_check_count = 0;
+}  // namespace
+
+bool register_check_reader(CheckReader reader)
+{
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    if (g_check_count < 16) g_check_readers[g_check_count++] = reader;
+    return true;
+}
+
+// The first failing record that mhc_device_status reported, kept until
+// mhc_testing_check_record reads it.
+std::mutex g_check_status_mu;
+CheckRecord g_last_check{};
+
+// Reads and clears every record; the first failing one goes to *first.
+cudaError_t read_and_clear_checks(CheckRecord *first)
+{
+    *first = CheckRecord{};
+    std::lock_guard<std::mutex> lock(g_check_mu);
+    for (int i = 0; i < g_check_count; ++i) {
+        CheckRecord rec{};
+        const cudaError_t e = g_check_readers[i](&rec);
+        if (e != cudaSuccess) return e;
+        if (rec.status != 0 && first->status == 0) *first = rec;
+    }
+    return cudaSuccess;
+}
+
+#ifdef MHC_CHECK
+namespace {
+__global__ void check_selftest_kernel(float *buf)
+{
+    constexpr int64_t kExtent = 16;
+    if (in_range(900, kExtent, 1, kExtent)) buf[kExtent] = 1.0f;  // refused: never stored
+}
+}  // namespace
+#endif
 
 cudaError_t current_device_info(DeviceInfo *info)
 {
@@ -334,6 +378,7 @@ const char *mhc_status_str(int status)
     case MHC_ERR_CUDA: return "MHC_ERR_CUDA: CUDA runtime call or launch failed";
     case MHC_ERR_TIMEOUT: return "MHC_ERR_TIMEOUT: a bounded device wait ran out";
     case MHC_ERR_WORKSPACE: return "MHC_ERR_WORKSPACE: workspace missing or too small";
+    case MHC_ERR_BOUNDS: return "MHC_ERR_BOUNDS: a device index check failed (MHC_CHECK build)";
     default: return "unknown mhc status";
     }
 }
@@ -846,14 +891,54 @@ int mhc_testing_memory_checks(int on)
     return g_memory_checks.exchange(on != 0 ? 1 : 0);
 }
 
+int mhc_testing_check_build(void) { return kCheckBuild ? 1 : 0; }
+
+int mhc_testing_check_record(int *site, int64_t *offset, int64_t *extent)
+{
+    if (site == nullptr || offset == nullptr || extent == nullptr) return MHC_ERR_INVALID;
+    std::lock_guard<std::mutex> lock(g_check_status_mu);
+    CheckRecord rec{};
+    if (read_and_clear_checks(&rec) != cudaSuccess) return MHC_ERR_CUDA;
+    if (g_last_check.status != 0) rec = g_last_check;  // seen first by mhc_device_status
+    g_last_check = CheckRecord{};
+    *site = rec.status != 0 ? rec.site : 0;
+    *offset = rec.status != 0 ? rec.off : 0;
+    *extent = rec.status != 0 ? rec.extent : 0;
+    return MHC_OK;
+}
+
+int mhc_testing_check_selftest(void)
+{
+#ifdef MHC_CHECK
+    float *buf = nullptr;
+    if (cudaMalloc(&buf, 16 * sizeof(float)) != cudaSuccess) return MHC_ERR_CUDA;
+    check_selftest_kernel<<<1, 1>>>(buf);
+    cudaError_t e = cudaGetLastError();
+    const cudaError_t s = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = s;
+    cudaFree(buf);
+    return cuda_status(e);
+#else
+    return MHC_ERR_UNSUPPORTED;
+#endif
+}
+
 int mhc_device_status(int *status)
 {
     if (status == nullptr) return MHC_ERR_INVALID;
-    int st[4] = {0, 0, 0, 0};
+    int st[5] = {0, 0, 0, 0, 0};
     if (read_and_clear_device_status(&st[0]) != cudaSuccess) return MHC_ERR_CUDA;
     if (read_and_clear_fused_status(&st[1]) != cudaSuccess) return MHC_ERR_CUDA;
     if (read_and_clear_decode_status(&st[2]) != cudaSuccess) return MHC_ERR_CUDA;
     if (read_and_clear_rmsnorm_gemm_status(&st[3]) != cudaSuccess) return MHC_ERR_CUDA;
+    if (kCheckBuild) {
+        // the records stay readable through mhc_testing_check_record
+        std::lock_guard<std::mutex> lock(g_check_status_mu);
+        CheckRecord rec{};
+        if (read_and_clear_checks(&rec) != cudaSuccess) return MHC_ERR_CUDA;
+        if (rec.status != 0 && g_last_check.status == 0) g_last_check = rec;
+        st[4] = g_last_check.status;
+    }
     *status = MHC_OK;
     for (int v : st)
         if (v != MHC_OK) {

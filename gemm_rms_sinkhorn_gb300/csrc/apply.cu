@@ -31,6 +31,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "check.cuh"
 #include "mhc_internal.h"
 #include "mix.cuh"
 #include "ptx.cuh"
@@ -49,10 +50,11 @@ __global__ void pre_apply_kernel(const uint16_t *__restrict__ X, const float *__
     ptx::pdl_wait();  // H_pre comes from the previous kernel
     ptx::pdl_trigger();
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        if (!in_range(101, b, 1, B)) continue;
         float h[n];
 #pragma unroll
         for (int i = 0; i < n; ++i) h[i] = __ldg(H_pre + b * n + i);
-        if (c8 < C8) {
+        if (c8 < C8 && in_range(102, c8 * 8, 8, C)) {
             const uint16_t *x = X + b * n * C + c8 * 8;
             uint4 xv[n];
 #pragma unroll
@@ -82,22 +84,21 @@ pre_apply_wide_kernel(const uint16_t *__restrict__ X, const float *__restrict__ 
         const int64_t bn = b + gridDim.y;
         const uint16_t *x = X + b * n * C + c8 * 8;
         uint4 xv[n];
-        if (active) {
+        if (!in_range(103, b, 1, B)) break;
+        const bool ok = active && in_range(104, c8 * 8, 8, C);
+        if (ok) {
 #pragma unroll
             for (int i = 0; i < n; ++i) xv[i] = ptx::ld_stream_v4(x + i * C);
         }
         float hn[n];
 #pragma unroll
         for (int i = 0; i < n; ++i) hn[i] = bn < B ? __ldg(H_pre + bn * n + i) : 0.f;
-        if (active) ptx::st_stream_v4(F_pre + b * C + c8 * 8, pre_mix8<n>(h, xv));
+        if (ok) ptx::st_stream_v4(F_pre + b * C + c8 * 8, pre_mix8<n>(h, xv));
 #pragma unroll
         for (int i = 0; i < n; ++i) h[i] = hn[i];
     }
 }
 
-// Up to n = 4 the kernel fits in 64 registers: 8 blocks of 128 threads per SM,
-// enough loads in flight to reach copy bandwidth (measured 305 µs against 312 µs
-// at 72 registers, B=16384, C=7168).  Wider n is held to 128 registers.
 // Eight consecutive F_out values as fp32, from bf16 (one 128-bit load) or fp32
 // (two) storage.
 __device__ __forceinline__ void load_f8(const uint16_t *p, float (&f)[8])
@@ -113,36 +114,39 @@ __device__ __forceinline__ void load_f8(const float *p, float (&f)[8])
     f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
 }
 
-// FT: the element type of F_out, uint16_t (bf16) or float.
+// n <= 4.  FT: the element type of F_out, uint16_t (bf16) or float.  The
+// kernel fits in 64 registers: 8 blocks of 128 threads per SM, enough loads in
+// flight to reach copy bandwidth (measured 305 µs against 312 µs at 72
+// registers, B=16384, C=7168).
 template <int n, typename FT>
-__global__ void __launch_bounds__(256, n <= 4 ? 4 : 2)
+__global__ void __launch_bounds__(256, 4)
 post_res_apply_kernel(const uint16_t *X, const FT *__restrict__ F_out,
-                                      const float *__restrict__ H_res,
-                                      const float *__restrict__ H_post, int64_t B, int64_t C,
-                                      uint16_t *X_next)
+                      const float *__restrict__ H_res, const float *__restrict__ H_post,
+                      int64_t B, int64_t C, uint16_t *X_next)
 {
+    static_assert(n <= 4, "wide n takes post_res_apply_wide_kernel");
     __shared__ float hs[n * n + n];
     const int64_t C8 = C >> 3;
     const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     ptx::pdl_wait();  // H_res and H_post come from earlier kernels
     ptx::pdl_trigger();
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+        const bool tok_ok = in_range(111, b, 1, B);
+        const bool ok = c8 < C8 && tok_ok && in_range(112, c8 * 8, 8, C);
         // the token's X and F_out are requested (into L2, no registers held)
-        // before its coefficients, so the two round trips overlap; wider n has
-        // no registers to spare for the addresses under its 128-register cap
-        if constexpr (n <= 4) {
-            if (c8 < C8) {
-                const uint16_t *x = X + b * n * C + c8 * 8;
+        // before its coefficients, so the two round trips overlap
+        if (ok) {
+            const uint16_t *x = X + b * n * C + c8 * 8;
 #pragma unroll
-                for (int j = 0; j < n; ++j) ptx::prefetch_l2(x + j * C);
-                ptx::prefetch_l2(F_out + b * C + c8 * 8);
-            }
+            for (int j = 0; j < n; ++j) ptx::prefetch_l2(x + j * C);
+            ptx::prefetch_l2(F_out + b * C + c8 * 8);
         }
         __syncthreads();  // previous token's coefficients are no longer read
         for (int t = threadIdx.x; t < n * n + n; t += blockDim.x)
-            hs[t] = t < n * n ? __ldg(H_res + b * n * n + t) : __ldg(H_post + b * n + (t - n * n));
+            if (tok_ok)
+                hs[t] = t < n * n ? __ldg(H_res + b * n * n + t) : __ldg(H_post + b * n + (t - n * n));
         __syncthreads();
-        if (c8 < C8) {
+        if (ok) {
             const uint16_t *x = X + b * n * C + c8 * 8;
             uint4 xv[n];
 #pragma unroll
@@ -175,7 +179,7 @@ post_res_apply_wide_kernel(const uint16_t *X, const FT *__restrict__ F_out,
     ptx::pdl_trigger();
     // coefficients of token bb into buffer k: H_res row-major, then H_post
     auto stage = [&](int64_t bb, int k) {
-        if (bb < B)
+        if (bb < B && in_range(121, bb, 1, B))
             for (int t = threadIdx.x; t < kH; t += blockDim.x)
                 ptx::cp_async4(&hs[k][t], t < n * n ? H_res + bb * n * n + t
                                                     : H_post + bb * n + (t - n * n));
@@ -190,7 +194,8 @@ post_res_apply_wide_kernel(const uint16_t *X, const FT *__restrict__ F_out,
         const uint16_t *x = X + b * n * C + c8 * 8;
         uint4 xv[n];
         float f[8];
-        if (active) {
+        const bool ok = active && in_range(122, b, 1, B) && in_range(123, c8 * 8, 8, C);
+        if (ok) {
 #pragma unroll
             for (int j = 0; j < n; ++j) xv[j] = ptx::ld_stream_v4(x + j * C);
             load_f8(F_out + b * C + c8 * 8, f);
@@ -198,12 +203,12 @@ post_res_apply_wide_kernel(const uint16_t *X, const FT *__restrict__ F_out,
         // buffer k ^ 1 was last read for token b - gridDim.y, before the
         // barrier that ended the previous step
         stage(bn, k ^ 1);
-        if (active && bn < B) {
+        if (ok && bn < B && in_range(124, bn, 1, B)) {
 #pragma unroll
             for (int j = 0; j < n; ++j) ptx::prefetch_l2(x + step + j * C);
             ptx::prefetch_l2(F_out + bn * C + c8 * 8);
         }
-        if (active) {
+        if (ok) {
             uint16_t *y = X_next + b * n * C + c8 * 8;
 #pragma unroll
             for (int i = 0; i < n; ++i) ptx::st_stream_v4(y + i * C, post_mix8<n>(hs[k], i, xv, f));

@@ -21,6 +21,7 @@
 
 #include <cstdint>
 
+#include "check.cuh"
 #include "mhc_internal.h"
 #include "ptx.cuh"
 
@@ -66,7 +67,7 @@ __global__ void pre_apply_e4m3_kernel(const uint8_t *__restrict__ X,
     const int64_t c16 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     ptx::pdl_wait();
     ptx::pdl_trigger();
-    if (c16 >= C16) return;
+    if (c16 >= C16 || !in_range(201, c16 * 16, 16, C)) return;
     constexpr int kT = kTokens<n>;
     const int64_t step = static_cast<int64_t>(gridDim.y);
     for (int64_t b0 = blockIdx.y; b0 < B; b0 += kT * step) {
@@ -76,14 +77,14 @@ __global__ void pre_apply_e4m3_kernel(const uint8_t *__restrict__ X,
         uint4 xv[kT][n];
 #pragma unroll
         for (int u = 0; u < kT; ++u)
-            if (bb[u] < B) {
+            if (bb[u] < B && in_range(202, bb[u], 1, B)) {
                 const uint8_t *x = X + bb[u] * n * C + c16 * 16;
 #pragma unroll
                 for (int i = 0; i < n; ++i) xv[u][i] = ptx::ld_stream_v4(x + i * C);
             }
 #pragma unroll
         for (int u = 0; u < kT; ++u) {
-            if (bb[u] >= B) break;
+            if (bb[u] >= B || !in_range(203, bb[u], 1, B)) break;
             uint32_t acc[8], t[8];
 #pragma unroll
             for (int p = 0; p < 8; ++p) acc[p] = 0u;  // +0, +0
@@ -110,7 +111,7 @@ post_res_apply_e4m3_kernel(const uint8_t *X, const uint8_t *__restrict__ F_out,
     __shared__ uint32_t hs[kT][kH];  // f16x2 (v, v): H_res row-major, then H_post, per token
     const int64_t C16 = C >> 4;
     const int64_t c16 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const bool active = c16 < C16;
+    const bool active = c16 < C16 && in_range(211, c16 * 16, 16, C);
     ptx::pdl_wait();
     ptx::pdl_trigger();
     const int64_t step = static_cast<int64_t>(gridDim.y);
@@ -118,13 +119,16 @@ post_res_apply_e4m3_kernel(const uint8_t *X, const uint8_t *__restrict__ F_out,
         int64_t bb[kT];
 #pragma unroll
         for (int u = 0; u < kT; ++u) bb[u] = b0 + u * step;
+        bool tok[kT];
+#pragma unroll
+        for (int u = 0; u < kT; ++u) tok[u] = bb[u] < B && in_range(212, bb[u], 1, B);
         uint4 xv[kT][n], fv[kT];
         if constexpr (kT > 1) {
             // all tokens' loads first, in flight while the coefficients are staged
             if (active) {
 #pragma unroll
                 for (int u = 0; u < kT; ++u)
-                    if (bb[u] < B) {
+                    if (tok[u]) {
                         const uint8_t *x = X + bb[u] * n * C + c16 * 16;
 #pragma unroll
                         for (int j = 0; j < n; ++j) xv[u][j] = ptx::ld_stream_v4(x + j * C);
@@ -135,7 +139,7 @@ post_res_apply_e4m3_kernel(const uint8_t *X, const uint8_t *__restrict__ F_out,
         __syncthreads();  // the previous tokens' coefficients are no longer read
         for (int t = threadIdx.x; t < kT * kH; t += blockDim.x) {
             const int u = t / kH, k = t - u * kH;
-            if (bb[u] < B)
+            if (bb[u] < B && in_range(213, bb[u], 1, B))
                 hs[u][k] = f16x2_splat(k < n * n ? __ldg(H_res + bb[u] * n * n + k)
                                                  : __ldg(H_post + bb[u] * n + (k - n * n)));
         }
@@ -143,7 +147,7 @@ post_res_apply_e4m3_kernel(const uint8_t *X, const uint8_t *__restrict__ F_out,
         if (!active) continue;
 #pragma unroll
         for (int u = 0; u < kT; ++u) {
-            if (bb[u] >= B) break;
+            if (!tok[u]) break;
             uint32_t xh[n][8], fh[8];
             if constexpr (kT > 1) {
 #pragma unroll

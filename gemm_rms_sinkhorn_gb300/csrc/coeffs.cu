@@ -15,6 +15,7 @@
 
 #include <cstdint>
 
+#include "check.cuh"
 #include "mhc_internal.h"
 #include "mix.cuh"
 #include "ptx.cuh"
@@ -36,6 +37,7 @@ coeffs_kernel(const float *__restrict__ Y, const float *__restrict__ r, float a_
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
     for (int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x; t < B;
          t += stride) {
+        if (!in_range(301, t, 1, B)) break;  // Y, r and the three outputs: row t
         float y[N];
         if constexpr (N % 4 == 0) {
             const float4 *src = reinterpret_cast<const float4 *>(Y + t * N);
@@ -70,7 +72,7 @@ __global__ void recip_kernel(const float *__restrict__ in, float *__restrict__ o
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
          i += stride)
-        out[i] = recip_approx(in[i]);
+        if (in_range(302, i, 1, count)) out[i] = recip_approx(in[i]);
 }
 
 }  // namespace

@@ -27,6 +27,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "check.cuh"
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
 #include "mix.cuh"
@@ -113,6 +114,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
     const int lane = threadIdx.x & 31;
     const int cta = blockIdx.x;
     const int64_t K = n * C;
+    // partial rows of the workspace: one slot of kBM rows per CTA and tile
+    const int64_t part_rows = (static_cast<int64_t>(sch.grid) + sch.m_tiles) * kBM;
     // this CTA's items for phases 2-3 (64-bit divisions: done here, before the
     // previous kernel has finished, not on the path after the grid barrier)
     const int64_t C8 = C >> 3;
@@ -154,12 +157,15 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
         Segment sg;
         while (it.next(sg)) {
             const int64_t grow = static_cast<int64_t>(sg.m) * kBM + row;
-            float *mine = partials + (static_cast<int64_t>(cta + sg.m) * kBM + row) * V;
+            const int64_t prow = static_cast<int64_t>(cta + sg.m) * kBM + row;
+            float *mine = partials + prow * V;
+            // a row past B stores nothing; one inside must have its slot
+            const bool keep = grow < B && in_range(601, prow, 1, part_rows);
             float ss;
             if constexpr (kSplit) {
                 const bool ok = pipe::take_accumulator_chunked<NPAD>(
                     p, seg, q, lane, ss, [&](int c, const float (&v)[32]) {
-                        if (grow >= B) return;
+                        if (!keep) return;
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             if (c * 16 + e < N) mine[c * 16 + e] = v[2 * e] + v[2 * e + 1];
@@ -168,14 +174,14 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
             } else {
                 float v[NPAD];
                 if (!pipe::take_accumulator<NPAD>(p, seg, q, lane, v, ss)) break;
-                if (grow < B) {
+                if (keep) {
 #pragma unroll
                     for (int j = 0; j < NPAD; ++j)
                         if (j < N) mine[j] = v[j];
                 }
             }
             ++seg;
-            if (grow < B) mine[N] = ss;
+            if (keep) mine[N] = ss;
         }
     }
     // lane 0 of the TMA and MMA warps ran alone: reconverge every warp before
@@ -214,7 +220,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
         const int cnt = static_cast<int>(t_last - t0 + 1 < nb ? t_last - t0 + 1 : nb);
         if (threadIdx.x < cnt) {
             const int64_t t = t0 + threadIdx.x;
-            const int m = static_cast<int>(t / kBM);
+            int m = static_cast<int>(t / kBM);
+            if (!in_range(602, m, 1, sch.m_tiles < kMaxTiles ? sch.m_tiles : kMaxTiles)) m = 0;
             int *ti = tinfo + threadIdx.x * 4;
             ti[0] = tc.first[m];
             ti[1] = tc.last[m];
@@ -235,7 +242,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int last = ti[1], m = ti[2], row = ti[3];
             const int c0 = ti[0] + s * kSegLen;
             float acc = 0.f;
-            if (c0 <= last) {
+            if (c0 <= last && in_range(603, (static_cast<int64_t>(last + m) * kBM + row), 1,
+                                       part_rows)) {
                 float vals[kSegLen];
 #pragma unroll
                 for (int u = 0; u < kSegLen; ++u)
@@ -246,7 +254,7 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
 #pragma unroll
                 for (int u = 1; u < kSegLen; ++u) acc += vals[u];
             }
-            red[pi] = acc;
+            if (in_range(604, pi, 1, kRedFloats)) red[pi] = acc;
         }
         __syncthreads();
         // second level: the segments in index order; Y and r of owned tokens
@@ -256,7 +264,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
             const int segs_t = (tinfo[j * 4 + 1] - tinfo[j * 4] + kSegLen) / kSegLen;
             float tot = red[qv];
             for (int s = 1; s < segs_t; ++s) tot += red[s * cnt * V + qv];
-            const bool owner = t * C8 >= lo;  // this CTA holds the token's first item
+            // this CTA holds the token's first item
+            const bool owner = t * C8 >= lo && in_range(605, t, 1, B);
             if (v < N) {
                 yv[qv] = tot;
                 if (owner) Y[t * N + v] = tot;
@@ -281,7 +290,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                 float hp[n], hq[n], mres[n][n];
                 token_coeffs<n>(yv + lane * V, yv[lane * V + N], bias_s, a_pre, a_post, a_res,
                                 iters, hp, hq, mres);
-                if (t * C8 >= lo) store_token_coeffs<n>(t, hp, hq, mres, H_pre, H_post, H_res);
+                if (t * C8 >= lo && in_range(606, t, 1, B))
+                    store_token_coeffs<n>(t, hp, hq, mres, H_pre, H_post, H_res);
             }
         } else {
             // F_pre of this CTA's items of these tokens, token by token, kU
@@ -297,6 +307,7 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                 for (int i = 0; i < n; ++i) h[i] = hps[j * n + i];
                 const uint16_t *xt = X + t * n * C;
                 uint16_t *ft = F_pre + t * C;
+                if (!in_range(607, t, 1, B) || !in_range(608, a * 8, (b > a ? b - a : 0) * 8, C)) continue;
                 for (int64_t c0 = a + threadIdx.x; c0 < b; c0 += kMixThreads * kU) {
                     uint4 xv[kU][n];
 #pragma unroll

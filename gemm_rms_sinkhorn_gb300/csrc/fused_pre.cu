@@ -38,6 +38,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "check.cuh"
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
 #include "mix.cuh"
@@ -238,8 +239,9 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
     const int j = g / fs.P, pc = g - (g / fs.P) * fs.P;  // tile slot, contributor
     const int G = fs.CH * fs.P;
     const int r0 = kBM * pc / fs.P, r1 = kBM * (pc + 1) / fs.P;  // rows this CTA finishes
-    // one CTA's partial: [kBM][N + 1] (N sums of Y, then Σx²)
+    // one CTA's partial: [kBM][N + 1] (N sums of Y, then Σx²); nb·G of them
     const int64_t part_stride = static_cast<int64_t>(kBM) * stride;
+    const int64_t part_slots = static_cast<int64_t>(fs.nb) * G;
 
     if (threadIdx.x == 0) {
         pipe::init_barriers(p);
@@ -297,6 +299,11 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int rb = fseg % kRowBufs;
             float *rows = rows_buf + rb * kMaxRows * stride;
             if (!pipe::wait(p, &rows_empty[rb], ((fseg / kRowBufs) & 1) ^ 1)) return false;
+            if (!in_range(501, t, 1, fs.m_tiles) ||
+                !in_range(502, static_cast<int64_t>(c % fs.nb) * G + static_cast<int64_t>(j) * fs.P,
+                          fs.P, part_slots) ||
+                !in_range(503, row0 + r0, nrows, B))
+                return false;
             if (et == 0) wait_count(p, &tickets[t], fs.P);
             // the acquire above and the group barrier order the partial loads
             if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) return false;
@@ -354,6 +361,11 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int64_t row0 = static_cast<int64_t>(t) * kBM;
             const int valid = static_cast<int>(B - row0 < kBM ? B - row0 : kBM);
 
+            if (!in_range(504, t, 1, fs.m_tiles) ||
+                !in_range(505, static_cast<int64_t>(c % fs.nb) * G + g, 1, part_slots)) {
+                ok = false;
+                break;
+            }
             // this buffer was last used for tile t - nb·CH: wait for its P readers
             if (c >= fs.nb && et == 0) wait_count(p, &done[t - fs.nb * fs.CH], fs.P);
             if (!pipe::group_sync(p, epi_bar, epi_phase) || *p.abort) {
@@ -428,13 +440,14 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
 #pragma unroll
                 for (int k = 0; k < n; ++k) h[k] = hp_buf[tk * 8 + k];
                 const int64_t tok = row0 + r0 + tk;
+                const bool tok_ok = in_range(506, tok, 1, B);
                 for (int c0 = 0; c0 < C; c0 += W) {
                     const int wp = C - c0 < W ? C - c0 : W;
                     if (!pipe::wait(p, &slot_full[slot], slot_phase)) {
                         ok = false;
                         break;
                     }
-                    if (pt * 8 < wp) {
+                    if (pt * 8 < wp && tok_ok && in_range(507, c0 + pt * 8, 8, C)) {
                         const uint8_t *sl = slots + slot * kSlotBytes;
                         uint4 xv[n];
 #pragma unroll
@@ -465,6 +478,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             const int rb = seg % kRowBufs;
             if (!pipe::wait(p, &rows_full[rb], (seg / kRowBufs) & 1)) break;
             for (int tk = lane; tk < nrows; tk += 32) {
+                if (!in_range(508, row0 + r0 + tk, 1, B)) break;
                 const float *yrow = rows_buf + (rb * kMaxRows + tk) * stride;
                 float hp[n], hq[n], m[n][n];
                 token_coeffs<n>(yrow, yrow[N], bias, a_pre, a_post, a_res, iters, hp, hq, m);
@@ -495,6 +509,7 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
             }
             for (int tk = 0; tk < nrows && ok; ++tk) {
                 const uint16_t *xrow = X + (row0 + r0 + tk) * K;
+                const bool row_ok = in_range(509, row0 + r0 + tk, 1, B);
                 for (int c0 = 0; c0 < C; c0 += W) {
                     const int wp = C - c0 < W ? C - c0 : W;
                     if (!pipe::wait(p, &slot_empty[slot], slot_phase ^ 1)) {
@@ -502,11 +517,17 @@ fused_pre_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant
                         break;
                     }
                     uint8_t *sl = slots + slot * kSlotBytes;
-                    ptx::mbar_arrive_expect_tx(&slot_full[slot], static_cast<uint32_t>(n * wp * 2));
+                    // a refused copy arrives without bytes: its reader skips it
+                    const bool copy_ok = row_ok && in_range(510, c0, wp, C) &&
+                                         in_range(511, 0, n * wp * 2, kSlotBytes);
+                    ptx::mbar_arrive_expect_tx(&slot_full[slot],
+                                               copy_ok ? static_cast<uint32_t>(n * wp * 2) : 0u);
+                    if (copy_ok) {
 #pragma unroll
-                    for (int k = 0; k < n; ++k)
-                        ptx::bulk_load(sl + k * wp * 2, xrow + static_cast<int64_t>(k) * C + c0,
-                                       static_cast<uint32_t>(wp * 2), &slot_full[slot], pol);
+                        for (int k = 0; k < n; ++k)
+                            ptx::bulk_load(sl + k * wp * 2, xrow + static_cast<int64_t>(k) * C + c0,
+                                           static_cast<uint32_t>(wp * 2), &slot_full[slot], pol);
+                    }
                     if (++slot == kSlots) { slot = 0; slot_phase ^= 1; }
                 }
             }

@@ -28,6 +28,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "check.cuh"
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
 #include "mix.cuh"
@@ -120,11 +121,11 @@ __device__ __forceinline__ void pair_coeffs_n(const CoefArgs &cf, const float *y
 // 0 and stores nothing.
 template <int NPAD, bool kSplit>
 __device__ __forceinline__ void tile_coeffs_share(const CoefArgs &cf, const float *rowbuf, int rs,
-                                                  int N, int K, int64_t row0, int rows, int g,
-                                                  int gt)
+                                                  int N, int K, int64_t row0, int rows, int64_t B,
+                                                  int g, int gt)
 {
     const int tk = g * 64 + (gt >> 1);
-    const bool live = tk < rows;
+    const bool live = tk < rows && in_range(409, row0 + tk, 1, B);
     const float *yr = rowbuf + (live ? tk : 0) * rs;
     const float rb = sqrtf(yr[N] / static_cast<float>(K));
 #define MHC_PAIR(k) pair_coeffs_n<NPAD, kSplit, k>(cf, yr, rb, gt & 1, live, row0 + tk);
@@ -201,7 +202,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                 const int64_t row0 = static_cast<int64_t>(m1 - 1) * kBM;
                 const int rows = static_cast<int>((B - row0) < kBM ? (B - row0) : kBM);
                 tile_coeffs_share<NPAD, kSplit>(cf, reinterpret_cast<const float *>(p.stages),
-                                                (N + 1) | 1, N, K, row0, rows, 1,
+                                                (N + 1) | 1, N, K, row0, rows, B, 1,
                                                 threadIdx.x - 64);
             }
         }
@@ -222,6 +223,8 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             const int stride = N + 1;
             // a partial is column-major, [N + 1][kBM]: stores and loads coalesce
             float *mine = partials + static_cast<int64_t>(cta + sg.m) * kBM * stride;
+            const int slots = sch.grid + sch.m_tiles;  // partial slots of the workspace
+            if (!whole && !in_range(401, cta + sg.m, 1, slots)) break;
             float ss;
             if constexpr (kSplit) {
                 // chunks of 32 accumulator columns = 16 weight columns
@@ -280,6 +283,10 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
             if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
             const int first = sch.owner(static_cast<int64_t>(sg.m) * sch.kbt);
             const int last = sch.owner(static_cast<int64_t>(sg.m + 1) * sch.kbt - 1);
+            // the tile's ticket and its contributors' slots first + m .. last + m
+            if (!in_range(402, sg.m, 1, sch.m_tiles) ||
+                !in_range(403, first + sg.m, last - first + 1, slots))
+                break;
             if (et == 0) {
                 const int prev = atomicAdd(&tile_tickets[sg.m], 1);
                 *is_last = (prev == last - first);
@@ -308,10 +315,12 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     float *rowbuf = reinterpret_cast<float *>(p.stages);  // [kBM][rs]
                     float *const chunk0 = rowbuf + kBM * rs;  // two buffers, [nc][cc][kBM]
                     const int64_t half = static_cast<int64_t>(nc) * cc * kBM;
+                    if (!in_range(404, 0, kBM * rs + 2 * half, C::kRingBytes / 4)) break;
                     const int nchunks = (stride + cc - 1) / cc;
                     auto issue = [&](int k) {
                         const int c0 = k * cc;
                         const int w = min(cc, stride - c0);
+                        if (!in_range(405, c0, w, stride)) return;  // its wait then runs out
                         const uint32_t bytes = static_cast<uint32_t>(w) * kBM * 4;
                         ptx::mbar_arrive_expect_tx(red_bar + (k & 1), bytes * nc);
                         for (int c = 0; c < nc; ++c)
@@ -382,6 +391,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         const int srow = 4 * kEpiThreads / N, scol = 4 * kEpiThreads % N;
                         int yr = 4 * et / N, yc = 4 * et % N;
                         for (int q4 = et; q4 < quads; q4 += kEpiThreads) {
+                            if (!in_range(406, row0 * N + 4 * q4, 4, B * N)) break;
                             float f[4];
 #pragma unroll
                             for (int u = 0; u < 4; ++u) {
@@ -406,7 +416,7 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                         if (et == 0) *coef_tile = static_cast<int>(sg.m) + 1;
                         ptx::mbar_arrive(coef_bar);
                         coef_arrived = true;
-                        tile_coeffs_share<NPAD, kSplit>(cf, rowbuf, rs, N, K, row0, rows, 0, et);
+                        tile_coeffs_share<NPAD, kSplit>(cf, rowbuf, rs, N, K, row0, rows, B, 0, et);
                     }
                     continue;
                 }
@@ -578,6 +588,7 @@ __global__ void split_phi_kernel(const float *__restrict__ phi_t, int64_t N, int
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t k = i / K, q = i - k * K;
+        if (!in_range(407, 2 * k + 1, 1, 2 * N)) break;
         const float v = phi_t[i];
         const uint32_t hi2 = pack_bf16_rn(v, 0.f);
         const float hi = __uint_as_float(hi2 << 16);

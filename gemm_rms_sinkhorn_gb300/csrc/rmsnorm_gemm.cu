@@ -32,6 +32,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "check.cuh"
 #include "gemm_pipeline.cuh"
 #include "mhc_internal.h"
 #include "ptx.cuh"
@@ -262,8 +263,10 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
                 if (grow < M && c0 < N) {
                     if (whole) {
                         const int valid = N - c0 < 32 ? static_cast<int>(N - c0) : 32;
-                        store_cols32(v, rstd, Cout + grow * N + c0, valid);
-                    } else {
+                        if (in_range(701, grow, 1, M) && in_range(702, c0, (valid + 7) / 8 * 8, N))
+                            store_cols32(v, rstd, Cout + grow * N + c0, valid);
+                    } else if (in_range(703, cta + tile, 1,
+                                        static_cast<int64_t>(sch.grid) + sch.tiles)) {
 #pragma unroll
                         for (int e = 0; e < 32; ++e) mine[row * stride + j * 32 + e] = v[e];
                     }
@@ -282,6 +285,10 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
             const int first = sch.owner(tile * sch.kbt);
             const int last = sch.owner((tile + 1) * sch.kbt - 1);
+            if (!in_range(704, tile, 1, sch.tiles) ||
+                !in_range(705, first + tile, last - first + 1,
+                          static_cast<int64_t>(sch.grid) + sch.tiles))
+                break;
             if (et == 0) {
                 const int prev = atomicAdd(&tickets[tile], 1);
                 *is_last = (prev == last - first);
@@ -308,6 +315,7 @@ rmsnorm_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
             for (int i = et; i < items; i += kEpiThreads) {
                 const int rr = i / (NT / 8), cc = (i - rr * (NT / 8)) * 8;
                 if (cc >= cols) continue;
+                if (!in_range(706, row0 + rr, 1, M) || !in_range(707, col0 + cc, 8, N)) continue;
                 float a8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) a8[e] = 0.f;
@@ -634,7 +642,8 @@ rmsnorm_gemm_m256_kernel(const __grid_constant__ CUtensorMap tm_a,
                     const int64_t c0 = col0 + j * 32;
                     if (grow < M && c0 < N) {
                         const int valid = N - c0 < 32 ? static_cast<int>(N - c0) : 32;
-                        store_cols32(v, rstd, Cout + grow * N + c0, valid);
+                        if (in_range(708, grow, 1, M) && in_range(709, c0, (valid + 7) / 8 * 8, N))
+                            store_cols32(v, rstd, Cout + grow * N + c0, valid);
                     }
                     __syncwarp();  // the next tcgen05.ld is warp-collective
                 }

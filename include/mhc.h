@@ -81,7 +81,8 @@ typedef enum {
     MHC_ERR_ALIGN = -3,       /* a pointer is not 16-byte aligned */
     MHC_ERR_CUDA = -4,        /* a CUDA runtime call or a kernel launch failed */
     MHC_ERR_TIMEOUT = -5,     /* a bounded device wait ran out (see mhc_device_status) */
-    MHC_ERR_WORKSPACE = -6    /* workspace NULL or smaller than mhc_workspace_bytes() */
+    MHC_ERR_WORKSPACE = -6,   /* workspace NULL or smaller than mhc_workspace_bytes() */
+    MHC_ERR_BOUNDS = -7       /* MHC_CHECK builds only: a device index check failed */
 } mhc_status;
 
 /* Human-readable name of a status code (static string, never NULL). */
@@ -344,7 +345,10 @@ int mhc_gemm_rms_noalloc(const mhc_bf16 *X, const mhc_bf16 *phi_t, int64_t B, in
 /*
  * Reads and clears the device status word of the current device: MHC_OK, or
  * MHC_ERR_TIMEOUT when a bounded wait inside a kernel ran out since the last
- * read (the kernel then stopped early, so its outputs are not valid).
+ * read (the kernel then stopped early, so its outputs are not valid).  A
+ * library built with -DMHC_CHECK also reports MHC_ERR_BOUNDS when a device
+ * index check failed since the last read (the access was skipped, so the
+ * outputs are not valid either); the default build has no such checks.
  * Blocks until all prior work on the device has finished.  Returns MHC_OK or
  * MHC_ERR_CUDA; the status is written to *status.
  */

@@ -119,6 +119,30 @@ int mhc_testing_host_chunks(int64_t B, int64_t *sizes, int64_t capacity, int64_t
  */
 int mhc_testing_memory_checks(int on);
 
+/*
+ * 1 if the library was built with -DMHC_CHECK (device index checks that
+ * record a failure and skip the access instead of faulting), else 0.
+ */
+int mhc_testing_check_build(void);
+
+/*
+ * Reads and clears the device index-check records of every translation unit
+ * (waits for the device first).  *site = the first failing site (0: none),
+ * *offset and *extent = its element offset and the buffer's element count.
+ * MHC_ERR_INVALID for a NULL pointer, MHC_ERR_CUDA if a copy fails.  In the
+ * default build every record is empty.
+ */
+int mhc_testing_check_record(int *site, int64_t *offset, int64_t *extent);
+
+/*
+ * Check build only: launches one thread that asks for element `extent` of a
+ * 16-element device buffer it owns (one past the end), which the check
+ * refuses and records as site 900 without touching memory.  Returns MHC_OK
+ * after the launch, MHC_ERR_UNSUPPORTED in the default build (which would
+ * not check), MHC_ERR_CUDA on a launch failure.
+ */
+int mhc_testing_check_selftest(void);
+
 #ifdef __cplusplus
 }
 #endif
