@@ -48,7 +48,7 @@ KERNELS = ("gemm_rms", "pre_apply", "post_res_apply")
 KERNEL_SOURCES = {"gemm_rms": "gemm_rms.cu", "pre_apply": "apply.cu",
                   "post_res_apply": "apply.cu"}
 # Kernels one prefill forward step launches (the chain, far above the small-batch
-# threshold of 3072 tokens): zero_tickets_kernel (the split-K tile counters of the
+# threshold of 2048 tokens): zero_tickets_kernel (the split-K tile counters of the
 # caller's workspace), gemm_rms_kernel, pre_apply_kernel and post_res_apply_kernel.
 LAUNCHES_PER_STEP = 4
 

@@ -90,6 +90,7 @@ _SIGS = {
     "mhc_testing_check_record": ([ctypes.POINTER(_i32), ctypes.POINTER(_i64),
                                   ctypes.POINTER(_i64)], _i32),
     "mhc_testing_check_selftest": ([], _i32),
+    "mhc_testing_forward_path": ([_i64, _i32, _i64, ctypes.POINTER(_i32)], _i32),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -238,7 +239,8 @@ def mhc_testing_forward_fused(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res,
 
 def mhc_testing_forward_chain(X, phi_t, F_out, alpha_pre, alpha_post, alpha_res, bias, iters, B,
                               n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream=None):
-    """Test hook: mhc_forward through the four-kernel chain whatever the batch."""
+    """Test hook: mhc_forward through the kernel chain (GEMM with the coefficients, pre
+    apply, X_next) whatever the batch."""
     _forward_like("mhc_testing_forward_chain", X, phi_t, F_out, alpha_pre, alpha_post, alpha_res,
                   bias, iters, B, n, C, Y, r, H_pre, H_post, H_res, F_pre, X_next, ws, stream)
 
@@ -428,6 +430,14 @@ def mhc_device_status() -> int:
     st = _i32(0)
     _check(_lib.mhc_device_status(ctypes.byref(st)), "mhc_device_status")
     return st.value
+
+
+def mhc_testing_forward_path(B: int, n: int, C: int) -> str:
+    """The path mhc_forward takes for (B, n, C): "decode" (one launch for steps
+    1-4a) or "chain"; host-side logic only."""
+    p = _i32(0)
+    _check(_lib.mhc_testing_forward_path(B, n, C, ctypes.byref(p)), "mhc_testing_forward_path")
+    return "decode" if p.value == 1 else "chain"
 
 
 def mhc_testing_check_record() -> tuple:

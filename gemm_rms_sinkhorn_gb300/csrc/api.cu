@@ -207,11 +207,18 @@ size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
     } while (0)
 
 // Batches up to this size take the one-launch steps 1-4a kernel.  Measured on
-// GB300 against the kernel chain: about 2x faster up to 512 tokens (the
-// chain is bound by launch and reduction latency there), 10-45% faster at
-// 1024-2048 (n = 4 and 8, C = 256..7168); at 3072 the two are within 2%
-// (n = 4, C = 7168), and from 4096 the chain is faster.
-constexpr int64_t kDecodeMaxTokens = 3072;
+// GB300 against the kernel chain (µs per forward in a CUDA graph): 1.6-2.7x
+// faster up to 512 tokens (the chain is bound by launch and reduction latency
+// there), 17-43% faster at 1024 (n = 4, C = 7168 and n = 8, C = 4096), within
+// 2% at 2048; from 2560 the chain is as fast or faster (3-4% at 3072).
+constexpr int64_t kDecodeMaxTokens = 2048;
+
+// mhc_forward's own choice (and that of its fp32-weight form): the one-launch
+// steps 1-4a kernel up to kDecodeMaxTokens, else the kernel chain.
+bool takes_decode_path(int64_t B, int n, int64_t C)
+{
+    return B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C);
+}
 
 enum class Path {
     Auto,           // decode_pre for small batches, else the kernel chain
@@ -259,8 +266,7 @@ static cudaError_t launch_forward(const uint16_t *X, const uint16_t *phi_t, cons
                                   uint16_t *X_next, void *workspace, int num_sms, cudaStream_t s,
                                   Path path, uint64_t wait_limit_ns)
 {
-    if (path == Path::Auto)
-        path = B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C) ? Path::Decode : Path::Chain;
+    if (path == Path::Auto) path = takes_decode_path(B, n, C) ? Path::Decode : Path::Chain;
     cudaError_t e;
     if (path == Path::Fused) {
         // steps 1-4a in one kernel that reads X from HBM once
@@ -668,7 +674,7 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
     MHC_TRY(check_on_device(outs + 7, 1, info));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (B <= kDecodeMaxTokens && decode_pre_eligible(B, n, C)) {
+    if (takes_decode_path(B, n, C)) {
         e = launch_decode_pre(X, phi_split, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
                               C, Y, r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
                               kWaitLimitNs, 0, true);
@@ -892,6 +898,14 @@ int mhc_testing_memory_checks(int on)
 }
 
 int mhc_testing_check_build(void) { return kCheckBuild ? 1 : 0; }
+
+int mhc_testing_forward_path(int64_t B, int n, int64_t C, int *path)
+{
+    if (path == nullptr) return MHC_ERR_INVALID;
+    MHC_TRY(check_shape(B, n, C, true));
+    *path = B > 0 && takes_decode_path(B, n, C) ? 1 : 0;
+    return MHC_OK;
+}
 
 int mhc_testing_check_record(int *site, int64_t *offset, int64_t *extent)
 {

@@ -66,7 +66,7 @@ int mhc_testing_forward_chain(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mh
  * mhc_forward forced onto the small-batch path: steps 1-4a in one cooperative
  * launch (the split-K GEMM over all SMs, a bounded grid barrier, then each
  * CTA's fixed-order reduction, coefficients and F_pre), then the X_next
- * kernel.  mhc_forward takes this path by itself for B <= 3072; this hook
+ * kernel.  mhc_forward takes this path by itself for B <= 2048; this hook
  * takes it for any B <= 4096.  Same arguments, rules and outputs as
  * mhc_forward; MHC_ERR_UNSUPPORTED for B > 4096.
  */
@@ -142,6 +142,15 @@ int mhc_testing_check_record(int *site, int64_t *offset, int64_t *extent);
  * not check), MHC_ERR_CUDA on a launch failure.
  */
 int mhc_testing_check_selftest(void);
+
+/*
+ * Host only (no device needed): the path mhc_forward and mhc_forward_f32w take
+ * for (B, n, C), written to *path: 1 = the one-launch steps 1-4a kernel (small
+ * batches, B <= 2048), 0 = the kernel chain (GEMM with the coefficients, pre
+ * apply), each followed by the X_next kernel.  B = 0 gives 0 (nothing runs).
+ * Status codes as mhc_forward's shape checks; MHC_ERR_INVALID for a NULL path.
+ */
+int mhc_testing_forward_path(int64_t B, int n, int64_t C, int *path);
 
 #ifdef __cplusplus
 }

@@ -133,7 +133,7 @@ def test_forward_f32w_wider_n8():
 
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 6, 7, 8])
 def test_forward_f32w_chain_every_n(n):
-    """Above 3072 tokens the forward takes the kernel chain, whose split-weight GEMM forms
+    """Above 2048 tokens the forward takes the kernel chain, whose split-weight GEMM forms
     the coefficients in its finalize: one GEMM width per n (2N padded to 16)."""
     wl = WORKLOADS["tiny"].with_(B=3200, n=n, C=64, bias_std=0.3)
     forward_f32w(wl, seed=77 + n)
@@ -141,7 +141,7 @@ def test_forward_f32w_chain_every_n(n):
 
 @pytest.mark.parametrize("n", [1, 2, 3, 5, 6, 7])
 def test_forward_f32w_decode_every_n(n):
-    """Up to 3072 tokens the forward takes the one-launch small-batch path with the
+    """Up to 2048 tokens the forward takes the one-launch small-batch path with the
     split weight (its partial rows hold both halves of each column pair): every n."""
     wl = WORKLOADS["tiny"].with_(B=100, n=n, C=72, bias_std=0.3)
     forward_f32w(wl, seed=90 + n)
