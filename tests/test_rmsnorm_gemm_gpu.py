@@ -47,12 +47,12 @@ def check(C_gpu, A, B_t, eps, rows=None):
 
 
 # whole-tile (>= 152 tiles) and split-K (fewer tiles than SMs) schedules, every
-# column-tile width (32, 64, 128, 256), ragged rows, columns and K blocks.  With
-# 256-column tiles and X = ceil(M/256)·ceil(N/256): X >= 76 takes the CTA pairs
-# (shapes 9-11, one with an odd number of row tiles and a column tile cut
-# inside its second half), and X >= 152 with K >= 4096 the 256-row tiles
-# (ragged rows, K blocks and columns; then a last group of 4 row tiles after two
-# of 8 in the grouped tile order; then 4 row tiles in all, one short group)
+# column-tile width (32, 64, 128, 256), ragged rows, columns and K blocks
+# (shapes 9-11: an odd number of row tiles, a column tile cut inside its second
+# half).  With 256-column tiles and X = ceil(M/256)·ceil(N/256), X >= 152 with
+# K >= 4096 takes the 256-row tiles (ragged rows, K blocks and columns; then a
+# last group of 4 row tiles after two of 8 in the grouped tile order; then 4 row
+# tiles in all, one short group)
 SHAPES = [(128, 64, 32), (300, 72, 40), (1000, 520, 200), (4096, 512, 1024),
           (8192, 256, 8), (2048, 1024, 256), (513, 4104, 96), (20000, 128, 64),
           (2000, 520, 2560), (19000, 200, 696), (2500, 1000, 4000), (4000, 4104, 2504),
