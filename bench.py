@@ -381,6 +381,57 @@ def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out
             for i, k in enumerate(KERNELS)}
 
 
+def gemm_after(mhc, stream, steps, warmup, wl, X, phi_t, F_out, bias, out) -> dict:
+    """Median CUDA-event time (µs) of the GEMM entry point (steps 1-3) right after
+    each predecessor, issued back to back on one stream: what the L2 holds when the
+    GEMM starts (clean lines, or an earlier kernel's output still dirty) shows in
+    its time."""
+    import torch
+
+    B, n, C = wl.B, wl.n, wl.C
+    rd = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    wr = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def gemm():
+        mhc.mhc_gemm_rms_coeffs(X, phi_t, wl.alpha_pre, wl.alpha_post, wl.alpha_res, bias,
+                                wl.iters, B, n, C, out["Y"], out["r"], out["H_pre"],
+                                out["H_post"], out["H_res"], out["ws"], stream)
+
+    def post():
+        mhc.mhc_post_res_apply(X, F_out, out["H_res"], out["H_post"], B, n, C, out["X_next"],
+                               stream)
+
+    def pre():
+        mhc.mhc_pre_apply(X, out["H_pre"], B, n, C, out["F_pre"], stream)
+
+    def read512():
+        rd.sum(dtype=torch.int64)
+
+    def write512():
+        wr.fill_(3)
+
+    cases = {"gemm": [gemm], "post_res_apply": [post], "pre_apply": [pre],
+             "post_res_apply, then a 512 MB read": [post, read512],
+             "a 512 MB read": [read512], "a 512 MB write": [write512]}
+    res = {}
+    with torch.cuda.stream(stream):
+        for label, before in cases.items():
+            ts = []
+            for it in range(warmup + steps):
+                for f in before:
+                    f()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                gemm()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if it >= warmup:
+                    ts.append(e0.elapsed_time(e1) * 1000.0)
+            res[label] = statistics.median(ts)
+    return res
+
+
 def host_link_copy(h_X, h_F, h_out, X, F_out, out, stream):
     """One step's bytes over the host link with nothing else running: X and
     F_out host->device on `stream` while every output goes device->host on a
@@ -488,8 +539,10 @@ def main() -> int:
     ap.add_argument("--tokens", type=int, default=None,
                     help="latency and kernels modes: the workload with this many tokens instead")
     ap.add_argument("--mode", default="full",
-                    choices=["full", "kernels", "latency", "rmsnorm_gemm"],
+                    choices=["full", "kernels", "latency", "rmsnorm_gemm", "gemm_after"],
                     help="kernels: only the per-kernel loop (small runs for ncu captures); "
+                         "gemm_after: the GEMM's event time after each predecessor "
+                         "(another GEMM, the apply kernels, a 512 MB read or write); "
                          "latency: microseconds per mhc_forward (stream and CUDA graph); "
                          "rmsnorm_gemm: C = rmsnorm(A) @ B (Lazy Pre-Norm) on --gemm M,K,N")
     ap.add_argument("--gemm", default="16384,2048,2048",
@@ -591,6 +644,13 @@ def main() -> int:
                               "algorithmic_bytes": alg,
                               "GBps_graph": alg / (res["us_per_forward_graph"] * 1e-6) / 1e9}),
                   flush=True)
+        return 0
+
+    if args.mode == "gemm_after":
+        print(json.dumps({"mode": "gemm_after", "workload": wl.name,
+                          "us": gemm_after(mhc, stream, args.steps, args.warmup, wl, X, phi_t,
+                                           F_out, bias, out)}), flush=True)
+        sampler.stop()
         return 0
 
     if args.mode == "kernels":
