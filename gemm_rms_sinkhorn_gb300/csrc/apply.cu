@@ -130,7 +130,9 @@ post_res_apply_kernel(const uint16_t *X, const FT *__restrict__ F_out,
     const int64_t c8 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     ptx::pdl_wait();  // H_res and H_post come from earlier kernels
     ptx::pdl_trigger();
-    for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
+    // the last tokens first: pre_apply, which runs just before in mhc_forward,
+    // read them last, so part of their X is still in L2
+    for (int64_t b = B - 1 - blockIdx.y; b >= 0; b -= gridDim.y) {
         const bool tok_ok = in_range(111, b, 1, B);
         const bool ok = c8 < C8 && tok_ok && in_range(112, c8 * 8, 8, C);
         // the token's X and F_out are requested (into L2, no registers held)
@@ -178,19 +180,23 @@ post_res_apply_wide_kernel(const uint16_t *X, const FT *__restrict__ F_out,
     ptx::pdl_wait();  // H_res and H_post come from earlier kernels
     ptx::pdl_trigger();
     // coefficients of token bb into buffer k: H_res row-major, then H_post
-    auto stage = [&](int64_t bb, int k) {
-        if (bb < B && in_range(121, bb, 1, B))
+    auto stage = [&](bool live, int64_t bb, int k) {
+        if (live && in_range(121, bb, 1, B))
             for (int t = threadIdx.x; t < kH; t += blockDim.x)
                 ptx::cp_async4(&hs[k][t], t < n * n ? H_res + bb * n * n + t
                                                     : H_post + bb * n + (t - n * n));
         ptx::cp_async_commit();
     };
-    int64_t b = blockIdx.y;
-    stage(b, 0);
+    // The walk goes down from the last token: pre_apply, which runs just
+    // before in mhc_forward, read the last tokens last, and part of their X is
+    // still in L2.
+    int64_t b = B - 1 - blockIdx.y;
+    stage(b >= 0, b, 0);
     ptx::cp_async_wait_all();
     __syncthreads();
-    for (int k = 0; b < B; b += gridDim.y, k ^= 1) {
-        const int64_t bn = b + gridDim.y;
+    for (int k = 0; b >= 0; b -= gridDim.y, k ^= 1) {
+        const int64_t bn = b - gridDim.y;  // the walk's next token
+        const bool next = bn >= 0;
         const uint16_t *x = X + b * n * C + c8 * 8;
         uint4 xv[n];
         float f[8];
@@ -200,12 +206,12 @@ post_res_apply_wide_kernel(const uint16_t *X, const FT *__restrict__ F_out,
             for (int j = 0; j < n; ++j) xv[j] = ptx::ld_stream_v4(x + j * C);
             load_f8(F_out + b * C + c8 * 8, f);
         }
-        // buffer k ^ 1 was last read for token b - gridDim.y, before the
+        // buffer k ^ 1 was last read for the walk's previous token, before the
         // barrier that ended the previous step
-        stage(bn, k ^ 1);
-        if (ok && bn < B && in_range(124, bn, 1, B)) {
+        stage(next, bn, k ^ 1);
+        if (ok && next && in_range(124, bn, 1, B)) {
 #pragma unroll
-            for (int j = 0; j < n; ++j) ptx::prefetch_l2(x + step + j * C);
+            for (int j = 0; j < n; ++j) ptx::prefetch_l2(x - step + j * C);
             ptx::prefetch_l2(F_out + bn * C + c8 * 8);
         }
         if (ok) {
