@@ -279,6 +279,9 @@ gemm_rms_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant_
                     mine[N * kBM + row] = ss;
                 }
             }
+            // the finishing CTA may read this partial by bulk copy (the async
+            // proxy): order the generic stores for that proxy too, then release
+            asm volatile("fence.proxy.async.global;" ::: "memory");
             __threadfence();
             if (!pipe::group_sync(p, epi_bar, epi_phase)) break;
             const int first = sch.owner(static_cast<int64_t>(sg.m) * sch.kbt);
