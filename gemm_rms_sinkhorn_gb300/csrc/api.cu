@@ -213,6 +213,11 @@ size_t f32_bytes(int64_t count) { return static_cast<size_t>(count) * 4; }
 // 2% at 2048; from 2560 the chain is as fast or faster (3-4% at 3072).
 constexpr int64_t kDecodeMaxTokens = 2048;
 
+// Up to this batch the one-launch kernel also forms X_next (step 4b) from the
+// coefficients it holds; above it a kernel of its own does, with more loads in
+// flight per SM than the one-launch kernel's ten warps.
+constexpr int64_t kDecodeXnextMaxTokens = 256;
+
 // mhc_forward's own choice (and that of its fp32-weight form): the one-launch
 // steps 1-4a kernel up to kDecodeMaxTokens, else the kernel chain.
 bool takes_decode_path(int64_t B, int n, int64_t C)
@@ -273,9 +278,12 @@ static cudaError_t launch_forward(const uint16_t *X, const uint16_t *phi_t, cons
         e = launch_fused_pre(X, phi_t, a_pre, a_post, a_res, bias, iters, B, n, C, Y, r, H_pre,
                              H_post, H_res, F_pre, workspace, num_sms, s);
     } else if (path == Path::Decode || path == Path::DecodeStalled) {
+        // steps 1-4a in one launch, and 4b with them for the smallest batches
+        const bool with_4b = B <= kDecodeXnextMaxTokens;
         e = launch_decode_pre(X, phi_t, a_pre, a_post, a_res, bias, iters, B, n, C, Y, r, H_pre,
-                              H_post, H_res, F_pre, workspace, num_sms, s, wait_limit_ns,
-                              path == Path::DecodeStalled ? 1 : 0);
+                              H_post, H_res, F_pre, F_out, with_4b ? X_next : nullptr, workspace,
+                              num_sms, s, wait_limit_ns, path == Path::DecodeStalled ? 1 : 0);
+        if (with_4b) return e;
     } else {
         // steps 1-3: the GEMM's finalize forms the coefficients of each finished token
         e = launch_gemm_rms(X, phi_t, B, n, C, Y, r, workspace, num_sms, s, kWaitLimitNs, -1,
@@ -674,9 +682,13 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
     MHC_TRY(check_on_device(outs + 7, 1, info));
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
+    bool with_4b = false;
     if (takes_decode_path(B, n, C)) {
+        // steps 1-4a in one launch, and 4b with them for the smallest batches
+        with_4b = B <= kDecodeXnextMaxTokens;
         e = launch_decode_pre(X, phi_split, alpha_pre, alpha_post, alpha_res, bias, iters, B, n,
-                              C, Y, r, H_pre, H_post, H_res, F_pre, workspace, info.num_sms, s,
+                              C, Y, r, H_pre, H_post, H_res, F_pre, F_out,
+                              with_4b ? X_next : nullptr, workspace, info.num_sms, s,
                               kWaitLimitNs, 0, true);
     } else {
         e = launch_gemm_rms_split(X, phi_split, B, n, C, Y, r, workspace, info.num_sms, s,
@@ -684,7 +696,7 @@ int mhc_forward_f32w(const mhc_bf16 *X, const mhc_bf16 *phi_split, const float *
                                             H_pre, H_post, H_res));
         if (e == cudaSuccess) e = launch_pre_apply(X, H_pre, B, n, C, F_pre, s);
     }
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !with_4b)
         e = launch_post_res_apply_f32(X, F_out, H_res, H_post, B, n, C, X_next, s);
     return cuda_status(e);
 }

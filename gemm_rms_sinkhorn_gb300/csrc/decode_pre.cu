@@ -18,14 +18,19 @@
 //            token's first item writes Y, r, H_pre, H_post and H_res;
 //   phase 3  F_pre of its items from X, which phase 1 has just streamed
 //            through L2, by nine warps while the tenth runs the Sinkhorn
-//            iteration (F_pre needs only H_pre, a sigmoid of the totals).
-// X_next (§2.5 (2)) needs F_out, which in a layer only exists after F has run
-// on F_pre, so it stays a launch of its own (apply.cu).
+//            iteration (F_pre needs only H_pre, a sigmoid of the totals);
+//   phase 4  (when X_next is given) X_next (§2.5 (2)) of the same items, by
+//            all ten warps, once the Sinkhorn iteration has given H_res.
+//            mhc_forward takes F_out as an input, so it is there from the
+//            start (in a layer, where F_out = F(F_pre), the step entry points
+//            run S4b after F).  Each item is read and written by one thread
+//            only, so X_next may be X.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 #include <mutex>
+#include <type_traits>
 
 #include "check.cuh"
 #include "gemm_pipeline.cuh"
@@ -59,6 +64,8 @@ template <int n, bool kSplit>
 struct DCfg {
     static constexpr int N = n * n + 2 * n;
     static constexpr int V = N + 1;  // a partial row: N sums of products, then Σx²
+    static constexpr int kH = n * n + n;  // a token's H_res (row-major), then H_post
+    using FT = std::conditional_t<kSplit, float, uint16_t>;  // the element type of F_out
     static constexpr int NPAD = kSplit ? (2 * N + 15) / 16 * 16 : npad_for(n);
     using C = pipe::Cfg<NPAD, kRingBudget>;
     static constexpr int kBiasBytes = (N * 4 + 15) / 16 * 16;  // b, staged for phase 2
@@ -66,8 +73,8 @@ struct DCfg {
         1024 + C::kRingBytes + pipe::kSsBytes + pipe::kBarrierBytes + kBiasBytes;
     static_assert(kSmemBytes <= 227 * 1024, "shared memory");
     // phase 2 scratch reuses the stage ring
-    static_assert((kRedFloats + kTokBatch * V + kTokBatch * n + kTokBatch * 4) * 4 <=
-                      C::kRingBytes, "scratch");
+    static_assert((kRedFloats + kTokBatch * V + kTokBatch * n + kTokBatch * 4 + kTokBatch * kH) *
+                      4 <= C::kRingBytes, "scratch");
 };
 
 constexpr int kMaxTiles = kMaxTokens / kBM;
@@ -76,6 +83,21 @@ constexpr int kMaxTiles = kMaxTokens / kBM;
 struct TileCtas {
     int first[kMaxTiles], last[kMaxTiles];
 };
+
+// Eight consecutive F_out values as fp32, from bf16 (one 128-bit load) or fp32
+// (two) storage.
+__device__ __forceinline__ void load_f8(const uint16_t *p, float (&f)[8])
+{
+    unpack8(ptx::ld_stream_v4(p), f);
+}
+__device__ __forceinline__ void load_f8(const float *p, float (&f)[8])
+{
+    const uint4 a = ptx::ld_stream_v4(p), b = ptx::ld_stream_v4(p + 4);
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+    f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+    f[4] = __uint_as_float(b.x); f[5] = __uint_as_float(b.y);
+    f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
+}
 
 // Bounded spin until *ctr >= target; false when the limit ran out.
 __device__ bool wait_arrivals(const uint32_t *ctr, uint32_t target, uint64_t limit_ns)
@@ -91,18 +113,19 @@ __device__ bool wait_arrivals(const uint32_t *ctr, uint32_t target, uint64_t lim
 template <int n, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
 decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
-                  const __grid_constant__ CUtensorMap tm_w, const uint16_t *__restrict__ X,
+                  const __grid_constant__ CUtensorMap tm_w, const uint16_t *X,
                   int64_t B, int64_t C, Sched sch, const __grid_constant__ TileCtas tc,
                   int seg_max, float a_pre, float a_post, float a_res,
                   const float *__restrict__ bias, int iters, float *__restrict__ Y,
                   float *__restrict__ r, float *__restrict__ H_pre, float *__restrict__ H_post,
                   float *__restrict__ H_res, uint16_t *__restrict__ F_pre,
+                  const typename DCfg<n, kSplit>::FT *__restrict__ F_out, uint16_t *X_next,
                   float *__restrict__ partials, uint32_t *grid_bar, uint32_t bar_target,
                   uint64_t wait_limit_ns)
 {
     using D = DCfg<n, kSplit>;
     using Cf = typename D::C;
-    constexpr int N = D::N, V = D::V, NPAD = D::NPAD;
+    constexpr int N = D::N, V = D::V, NPAD = D::NPAD, kH = D::kH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -214,6 +237,7 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
     float *yv = red + kRedFloats;                      // [tokens][V]: Y row, then r
     float *hps = yv + kTokBatch * V;                   // [tokens][n]: H_pre
     int *tinfo = reinterpret_cast<int *>(hps + kTokBatch * n);  // [tokens]: first, last, m, row
+    float *hres = reinterpret_cast<float *>(tinfo + kTokBatch * 4);  // [tokens][kH]: H_res, H_post
     int nb = kRedFloats / (V * seg_max);
     if (nb > kTokBatch) nb = kTokBatch;
     for (int64_t t0 = t_first; t0 <= t_last; t0 += nb) {
@@ -292,6 +316,14 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                                 iters, hp, hq, mres);
                 if (t * C8 >= lo && in_range(606, t, 1, B))
                     store_token_coeffs<n>(t, hp, hq, mres, H_pre, H_post, H_res);
+                // for phase 4
+                float *hr = hres + lane * kH;
+#pragma unroll
+                for (int i = 0; i < n; ++i) {
+#pragma unroll
+                    for (int jj = 0; jj < n; ++jj) hr[i * n + jj] = mres[i][jj];
+                    hr[n * n + i] = hq[i];
+                }
             }
         } else {
             // F_pre of this CTA's items of these tokens, token by token, kU
@@ -315,14 +347,55 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                         const int64_t c8 = c0 + u * kMixThreads;
                         if (c8 < b) {
 #pragma unroll
-                            for (int i = 0; i < n; ++i)
-                                xv[u][i] = __ldg(reinterpret_cast<const uint4 *>(xt + i * C + c8 * 8));
+                            for (int i = 0; i < n; ++i)  // plain loads: X_next may be X
+                                xv[u][i] = *reinterpret_cast<const uint4 *>(xt + i * C + c8 * 8);
                         }
                     }
 #pragma unroll
                     for (int u = 0; u < kU; ++u) {
                         const int64_t c8 = c0 + u * kMixThreads;
                         if (c8 < b) ptx::st_stream_v4(ft + c8 * 8, pre_mix8<n>(h, xv[u]));
+                    }
+                }
+            }
+        }
+        if (X_next != nullptr) {
+            __syncthreads();  // H_res and H_post of the batch are in shared memory
+            // phase 4: X_next of this CTA's items of these tokens, by all ten
+            // warps, kV items a thread at a time so that their loads are in
+            // flight together; every item's loads come before its stores, in
+            // the same thread
+            constexpr int kV = n <= 3 ? 2 : 1;
+            for (int j = 0; j < cnt; ++j) {
+                const int64_t t = t0 + j;
+                const int64_t a = (t * C8 > lo ? t * C8 : lo) - t * C8;
+                const int64_t b = ((t + 1) * C8 < hi ? (t + 1) * C8 : hi) - t * C8;
+                if (!in_range(609, t, 1, B) || !in_range(610, a * 8, (b > a ? b - a : 0) * 8, C))
+                    continue;
+                const float *hr = hres + j * kH;
+                const uint16_t *xt = X + t * n * C;
+                const typename D::FT *fo = F_out + t * C;
+                uint16_t *yt = X_next + t * n * C;
+                for (int64_t c0 = a + threadIdx.x; c0 < b; c0 += kThreads * kV) {
+                    uint4 xv[kV][n];
+                    float f[kV][8];
+#pragma unroll
+                    for (int u = 0; u < kV; ++u) {
+                        const int64_t c8 = c0 + u * kThreads;
+                        if (c8 < b) {
+#pragma unroll
+                            for (int i = 0; i < n; ++i) xv[u][i] = ptx::ld_stream_v4(xt + i * C + c8 * 8);
+                            load_f8(fo + c8 * 8, f[u]);
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kV; ++u) {
+                        const int64_t c8 = c0 + u * kThreads;
+                        if (c8 < b) {
+#pragma unroll
+                            for (int i = 0; i < n; ++i)
+                                ptx::st_stream_v4(yt + i * C + c8 * 8, post_mix8<n>(hr, i, xv[u], f[u]));
+                        }
                     }
                 }
             }
@@ -377,9 +450,9 @@ cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_
                      int64_t C, const Sched &s, const TileCtas &tc, int seg_max, float a_pre,
                      float a_post,
                      float a_res, const float *bias, int iters, float *Y, float *r, float *H_pre,
-                     float *H_post, float *H_res, uint16_t *F_pre, float *partials,
-                     uint32_t *bar, uint32_t bar_target, uint64_t limit, int device,
-                     cudaStream_t stream)
+                     float *H_post, float *H_res, uint16_t *F_pre, const void *F_out,
+                     uint16_t *X_next, float *partials, uint32_t *bar, uint32_t bar_target,
+                     uint64_t limit, int device, cudaStream_t stream)
 {
     using D = DCfg<n, kSplit>;
     static uint64_t configured = 0;  // one bit per device
@@ -394,8 +467,9 @@ cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_
     }
     return launch_coop_pdl(decode_pre_kernel<n, kSplit>, dim3(s.grid), dim3(kThreads), D::kSmemBytes,
                            stream, tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias,
-                           iters,
-                           Y, r, H_pre, H_post, H_res, F_pre, partials, bar, bar_target, limit);
+                           iters, Y, r, H_pre, H_post, H_res, F_pre,
+                           static_cast<const typename D::FT *>(F_out), X_next, partials, bar,
+                           bar_target, limit);
 }
 
 }  // namespace
@@ -416,9 +490,9 @@ size_t decode_pre_workspace_bytes(int64_t B, int n, int64_t C, int num_sms)
 cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_pre, float a_post,
                               float a_res, const float *bias, int iters, int64_t B, int n,
                               int64_t C, float *Y, float *r, float *H_pre, float *H_post,
-                              float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
-                              cudaStream_t stream, uint64_t wait_limit_ns, int barrier_extra,
-                              bool split)
+                              float *H_res, uint16_t *F_pre, const void *F_out, uint16_t *X_next,
+                              void *workspace, int num_sms, cudaStream_t stream,
+                              uint64_t wait_limit_ns, int barrier_extra, bool split)
 {
     if (!decode_pre_eligible(B, n, C)) return cudaErrorInvalidValue;
     const int N = num_coeffs(n);
@@ -444,11 +518,12 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
     case k:                                                                                    \
         return split ? launch_n<k, true>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, \
                                          bias, iters, Y, r, H_pre, H_post, H_res, F_pre,       \
-                                         partials, bar, target, wait_limit_ns, device, stream) \
+                                         F_out, X_next, partials, bar, target, wait_limit_ns,  \
+                                         device, stream)                                       \
                      : launch_n<k, false>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post,      \
                                           a_res, bias, iters, Y, r, H_pre, H_post, H_res,      \
-                                          F_pre, partials, bar, target, wait_limit_ns, device, \
-                                          stream);
+                                          F_pre, F_out, X_next, partials, bar, target,         \
+                                          wait_limit_ns, device, stream);
         MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
         MHC_CASE(8)
 #undef MHC_CASE

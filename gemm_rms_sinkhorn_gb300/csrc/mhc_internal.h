@@ -117,12 +117,16 @@ size_t decode_pre_workspace_bytes(int64_t B, int n, int64_t C, int num_sms);
 // barrier_extra > 0 is a test hook: the grid barrier waits for that many
 // arrivals more than there are CTAs, so every CTA's wait runs out.  split:
 // phi_t is the fp32-weight form (bf16 pairs, 2N rows).
+// Steps 1-4a in one cooperative launch (small batches), and step 4b too when
+// X_next is not NULL.  F_out is bf16, or fp32 when split (the fp32-weight
+// forward); X_next may be X.
 cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_pre, float a_post,
                               float a_res, const float *bias, int iters, int64_t B, int n,
                               int64_t C, float *Y, float *r, float *H_pre, float *H_post,
-                              float *H_res, uint16_t *F_pre, void *workspace, int num_sms,
-                              cudaStream_t stream, uint64_t wait_limit_ns = kWaitLimitNs,
-                              int barrier_extra = 0, bool split = false);
+                              float *H_res, uint16_t *F_pre, const void *F_out, uint16_t *X_next,
+                              void *workspace, int num_sms, cudaStream_t stream,
+                              uint64_t wait_limit_ns = kWaitLimitNs, int barrier_extra = 0,
+                              bool split = false);
 cudaError_t read_and_clear_decode_status(int *status);
 
 // ---- the whole forward on device buffers (api.cu), arguments already valid

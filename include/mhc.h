@@ -13,8 +13,8 @@
  *   mhc_pre_apply       F_pre = Σ_i H_pre[i]·X[i]                 (§2.5)
  *   mhc_post_res_apply  X_next[i] = Σ_j H_res[i][j]·X[j] + H_post[i]·F_out (§2.5, §3.4)
  *   mhc_forward         steps 1-4b on one stream (mhc_gemm_rms_coeffs, mhc_pre_apply,
- *                       mhc_post_res_apply, or for B <= 2048 steps 1-4a in one
- *                       launch, then step 4b)
+ *                       mhc_post_res_apply; for B <= 2048 steps 1-4a in one
+ *                       launch, and 4b in it too for B <= 256)
  *   mhc_forward_host    mhc_forward over host buffers, copies overlapped with compute
  *   mhc_gemm_rms_coeffs steps 1-3 in one launch (mhc_gemm_rms then mhc_coeffs)
  *   mhc_rmsnorm_gemm    C = rmsnorm(A) @ B for any N (Lazy Pre-Norm, second page §2)
@@ -158,14 +158,15 @@ int mhc_post_res_apply(const mhc_bf16 *X, const mhc_bf16 *F_out, const float *H_
 /*
  * The whole forward on `stream`, with the same argument rules and results as
  * mhc_gemm_rms, mhc_coeffs, mhc_pre_apply and mhc_post_res_apply called in
- * that order.  F_out is an input: inside a real layer it is F(F_pre), which
- * lies outside mHC (§2.5 (2)), so step 4b is always a launch of its own.
- * X_next may be exactly X.
+ * that order.  F_out is an input, present from the start: inside a real layer
+ * it is F(F_pre), which lies outside mHC (§2.5 (2)), and such a layer calls the
+ * step entry points with F between them.  X_next may be exactly X.
  *
  * Path: for B <= 2048 steps 1-4a run as one cooperative launch (the split-K
  * GEMM over every SM, a bounded grid barrier, then each CTA's fixed-order
- * reduction, coefficients and F_pre), which measured faster than the
- * kernel chain at those sizes; above, the chain (mhc_gemm_rms_coeffs,
+ * reduction, coefficients and F_pre, and for B <= 256 X_next too; above 256
+ * mhc_post_res_apply follows), which measured faster than the kernel chain at
+ * those sizes; above 2048, the chain (mhc_gemm_rms_coeffs,
  * mhc_pre_apply, mhc_post_res_apply).  Either path is
  * deterministic; they differ in the split-K order, so Y (and what follows
  * from it) differs between them in the last bits, within the tolerances.
@@ -234,8 +235,8 @@ int mhc_forward_host(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mhc_bf16 *F
  *                       (same workspace as mhc_gemm_rms);
  *   mhc_post_res_apply_f32  mhc_post_res_apply with F_out [B][C] fp32;
  *   mhc_forward_f32w    the forward with both (X, F_pre, X_next bf16): like
- *                       mhc_forward, steps 1-4a in one launch for B <= 2048,
- *                       else the kernel chain; workspace of
+ *                       mhc_forward, steps 1-4a (1-4b up to 256) in one launch
+ *                       for B <= 2048, else the kernel chain; workspace of
  *                       mhc_workspace_bytes.
  * Rules, layouts and status codes otherwise as the bf16 calls.
  */

@@ -65,8 +65,9 @@ int mhc_testing_forward_chain(const mhc_bf16 *X, const mhc_bf16 *phi_t, const mh
 /*
  * mhc_forward forced onto the small-batch path: steps 1-4a in one cooperative
  * launch (the split-K GEMM over all SMs, a bounded grid barrier, then each
- * CTA's fixed-order reduction, coefficients and F_pre), then the X_next
- * kernel.  mhc_forward takes this path by itself for B <= 2048; this hook
+ * CTA's fixed-order reduction, coefficients and F_pre of its share of the
+ * channels), with X_next in it for B <= 256 and the X_next kernel after it
+ * above.  mhc_forward takes this path by itself for B <= 2048; this hook
  * takes it for any B <= 4096.  Same arguments, rules and outputs as
  * mhc_forward; MHC_ERR_UNSUPPORTED for B > 4096.
  */
@@ -145,9 +146,9 @@ int mhc_testing_check_selftest(void);
 
 /*
  * Host only (no device needed): the path mhc_forward and mhc_forward_f32w take
- * for (B, n, C), written to *path: 1 = the one-launch steps 1-4a kernel (small
- * batches, B <= 2048), 0 = the kernel chain (GEMM with the coefficients, pre
- * apply), each followed by the X_next kernel.  B = 0 gives 0 (nothing runs).
+ * for (B, n, C), written to *path: 1 = the one-launch kernel (small batches,
+ * B <= 2048: steps 1-4a, and 4b with them up to 256 tokens), 0 = the kernel
+ * chain (GEMM with the coefficients, pre apply, X_next).  B = 0 gives 0.
  * Status codes as mhc_forward's shape checks; MHC_ERR_INVALID for a NULL path.
  */
 int mhc_testing_forward_path(int64_t B, int n, int64_t C, int *path);
