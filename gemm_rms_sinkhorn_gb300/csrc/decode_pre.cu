@@ -28,8 +28,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <mutex>
+#include <random>
 #include <type_traits>
 
 #include "check.cuh"
@@ -99,12 +101,45 @@ __device__ __forceinline__ void load_f8(const float *p, float (&f)[8])
     f[6] = __uint_as_float(b.z); f[7] = __uint_as_float(b.w);
 }
 
-// Bounded spin until *ctr >= target; false when the limit ran out.
-__device__ bool wait_arrivals(const uint32_t *ctr, uint32_t target, uint64_t limit_ns)
+// The grid barrier's two words (arrivals, then departures) hold a launch's
+// 48-bit epoch above a 16-bit count.  CTA 0 writes (epoch, 0) to both as it
+// starts, once the previous kernel has finished, so the words need no clearing
+// beforehand.  An arrival is one atomic add; one that lands before CTA 0's
+// write (the old value carries another tag) is wiped out by that write and is
+// made again.  The last CTA to leave, and every CTA whose wait runs out, set
+// both words to 0, so no later launch meets this launch's tag, not even a
+// replay of the same CUDA graph, which reuses the epoch.
+constexpr int kCountBits = 16;
+constexpr unsigned long long kCountMask = (1ull << kCountBits) - 1;
+
+__device__ __forceinline__ bool tagged(unsigned long long v, unsigned long long epoch)
 {
-    const uint64_t t0 = ptx::globaltimer_ns();
+    return (v >> kCountBits) == epoch;
+}
+
+// Adds this CTA's arrival to *w for this epoch; false when the word did not
+// carry the epoch before the limit ran out (counted from t0).
+__device__ bool arrive(unsigned long long *w, unsigned long long epoch, uint64_t t0,
+                       uint64_t limit_ns)
+{
+    for (;;) {
+        if (tagged(atomicAdd(w, 1ull), epoch)) return true;
+        for (uint32_t polls = 0; !tagged(ptx::ld_acquire_gpu_u64(w), epoch); ++polls) {
+            if ((polls & 31) == 31 && ptx::globaltimer_ns() - t0 > limit_ns) return false;
+            __nanosleep(64);
+        }
+        if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Bounded spin until *w counts at least `target` for this epoch; false when
+// the limit ran out (counted from t0).
+__device__ bool wait_arrivals(const unsigned long long *w, unsigned long long epoch,
+                              uint32_t target, uint64_t t0, uint64_t limit_ns)
+{
     for (uint32_t polls = 0;; ++polls) {
-        if (ptx::ld_acquire_gpu(ctr) >= target) return true;
+        const unsigned long long v = ptx::ld_acquire_gpu_u64(w);
+        if (tagged(v, epoch) && (v & kCountMask) >= target) return true;
         if ((polls & 31) == 31 && ptx::globaltimer_ns() - t0 > limit_ns) return false;
         __nanosleep(32);
     }
@@ -120,8 +155,8 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
                   float *__restrict__ r, float *__restrict__ H_pre, float *__restrict__ H_post,
                   float *__restrict__ H_res, uint16_t *__restrict__ F_pre,
                   const typename DCfg<n, kSplit>::FT *__restrict__ F_out, uint16_t *X_next,
-                  float *__restrict__ partials, uint32_t *grid_bar, uint32_t bar_target,
-                  uint64_t wait_limit_ns)
+                  float *__restrict__ partials, unsigned long long *grid_bar,
+                  unsigned long long epoch, uint32_t bar_target, uint64_t wait_limit_ns)
 {
     using D = DCfg<n, kSplit>;
     using Cf = typename D::C;
@@ -160,6 +195,11 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
     ptx::tc_fence_after();
     p.tmem_base = *p.tmem_holder;
     ptx::pdl_wait();
+    if (cta == 0 && threadIdx.x == 0) {  // this launch's tag on the grid barrier's words
+        atomicExch(grid_bar + 1, epoch << kCountBits);
+        __threadfence();
+        atomicExch(grid_bar, epoch << kCountBits);
+    }
     // b for phase 2, fetched now so its latency hides behind phase 1
     for (int k = threadIdx.x; k < N; k += kThreads) bias_s[k] = __ldg(bias + k);
 
@@ -222,8 +262,24 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
     // 0's fence, which is cumulative: they are visible before its arrival.
     if (threadIdx.x == 0) {
         __threadfence();
-        atomicAdd(grid_bar, 1u);
-        if (!*p.abort && !wait_arrivals(grid_bar, bar_target, wait_limit_ns)) pipe::raise_timeout(p);
+        unsigned long long *departed = grid_bar + 1;
+        // A CTA whose phase 1 gave up still arrives and leaves like the
+        // others (they are all resident, so its wait is short) and returns
+        // below; only a wait that runs out clears the words early.
+        const uint64_t t0 = ptx::globaltimer_ns();
+        if (!arrive(grid_bar, epoch, t0, wait_limit_ns) ||
+            !wait_arrivals(grid_bar, epoch, bar_target, t0, wait_limit_ns)) {
+            atomicExch(grid_bar, 0ull);  // leave the words clear for the next launch
+            atomicExch(departed, 0ull);
+            pipe::raise_timeout(p);
+        } else {
+            const unsigned long long left = atomicAdd(departed, 1ull);
+            if (tagged(left, epoch) && (left & kCountMask) + 1 == gridDim.x) {
+                // every CTA has seen the barrier complete: clear it for the next launch
+                atomicExch(grid_bar, 0ull);
+                atomicExch(departed, 0ull);
+            }
+        }
     }
     __syncwarp();  // warp 0 whole again before the CTA barrier
     __syncthreads();
@@ -404,14 +460,6 @@ decode_pre_kernel(const __grid_constant__ CUtensorMap tm_x,
     }
 }
 
-// Clears the grid-barrier word before the kernel that counts on it.
-__global__ void zero_word_kernel(uint32_t *w)
-{
-    ptx::pdl_wait();
-    ptx::pdl_trigger();
-    *w = 0;
-}
-
 Sched decode_sched(int64_t B, int n, int64_t C, int num_sms)
 {
     Sched s;
@@ -445,14 +493,31 @@ int decode_seg_max(const Sched &s, const TileCtas &tc)
 
 constexpr size_t kBarBytes = 256;
 
+// A fresh 48-bit epoch per launch (never 0), from a process-wide counter that
+// starts at a random value, so a stale word from another process or an
+// earlier use of the memory matches it only by a 2^-48 chance.
+unsigned long long next_epoch()
+{
+    static std::atomic<unsigned long long> counter{[] {
+        std::random_device rd;
+        return (static_cast<unsigned long long>(rd()) << 32) ^ rd();
+    }()};
+    constexpr unsigned long long kMask = (1ull << (64 - kCountBits)) - 1;
+    for (;;) {
+        const unsigned long long e = counter.fetch_add(1, std::memory_order_relaxed) & kMask;
+        if (e != 0) return e;
+    }
+}
+
 template <int n, bool kSplit>
 cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_t *X, int64_t B,
                      int64_t C, const Sched &s, const TileCtas &tc, int seg_max, float a_pre,
                      float a_post,
                      float a_res, const float *bias, int iters, float *Y, float *r, float *H_pre,
                      float *H_post, float *H_res, uint16_t *F_pre, const void *F_out,
-                     uint16_t *X_next, float *partials, uint32_t *bar, uint32_t bar_target,
-                     uint64_t limit, int device, cudaStream_t stream)
+                     uint16_t *X_next, float *partials, unsigned long long *bar,
+                     unsigned long long epoch, uint32_t bar_target, uint64_t limit, int device,
+                     cudaStream_t stream)
 {
     using D = DCfg<n, kSplit>;
     static uint64_t configured = 0;  // one bit per device
@@ -469,7 +534,7 @@ cudaError_t launch_n(const CUtensorMap &tx, const CUtensorMap &tw, const uint16_
                            stream, tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, bias,
                            iters, Y, r, H_pre, H_post, H_res, F_pre,
                            static_cast<const typename D::FT *>(F_out), X_next, partials, bar,
-                           bar_target, limit);
+                           epoch, bar_target, limit);
 }
 
 }  // namespace
@@ -506,23 +571,23 @@ cudaError_t launch_decode_pre(const uint16_t *X, const uint16_t *phi_t, float a_
         !make_tmap(&tw, phi_t, static_cast<uint64_t>(K), static_cast<uint64_t>(wrows),
                    static_cast<uint32_t>((wrows + 15) / 16 * 16)))
         return cudaErrorInvalidValue;
-    uint32_t *bar = static_cast<uint32_t *>(workspace);
+    unsigned long long *bar = static_cast<unsigned long long *>(workspace);
     float *partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + kBarBytes);
-    cudaError_t e = launch_pdl(zero_word_kernel, dim3(1), dim3(1), 0, stream, bar);
-    if (e != cudaSuccess) return e;
+    const unsigned long long epoch = next_epoch();
     int device = 0;
-    if ((e = cudaGetDevice(&device)) != cudaSuccess) return e;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return e;
     const uint32_t target = static_cast<uint32_t>(s.grid + (barrier_extra > 0 ? barrier_extra : 0));
     switch (n) {
 #define MHC_CASE(k)                                                                            \
     case k:                                                                                    \
         return split ? launch_n<k, true>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post, a_res, \
                                          bias, iters, Y, r, H_pre, H_post, H_res, F_pre,       \
-                                         F_out, X_next, partials, bar, target, wait_limit_ns,  \
-                                         device, stream)                                       \
+                                         F_out, X_next, partials, bar, epoch, target,          \
+                                         wait_limit_ns, device, stream)                        \
                      : launch_n<k, false>(tx, tw, X, B, C, s, tc, seg_max, a_pre, a_post,      \
                                           a_res, bias, iters, Y, r, H_pre, H_post, H_res,      \
-                                          F_pre, F_out, X_next, partials, bar, target,         \
+                                          F_pre, F_out, X_next, partials, bar, epoch, target,  \
                                           wait_limit_ns, device, stream);
         MHC_CASE(1) MHC_CASE(2) MHC_CASE(3) MHC_CASE(4) MHC_CASE(5) MHC_CASE(6) MHC_CASE(7)
         MHC_CASE(8)

@@ -253,6 +253,13 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p)
     return v;
 }
 
+__device__ __forceinline__ unsigned long long ld_acquire_gpu_u64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // Blocks until the grids this one depends on (the previous kernel in the
 // stream, when launched with programmatic stream serialisation) have
 // completed and their memory is visible.  A no-op otherwise.

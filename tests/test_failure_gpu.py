@@ -13,7 +13,7 @@ import torch
 import oracle
 from gpu_util import (H_TOL, R_REL, assert_abs, assert_bf16_close, assert_rel, assert_Y_close,
                       cuda_ok, dev_bf16, dev_f32, host64, phi_KN)
-from synth import WORKLOADS, make_inputs
+from synth import WORKLOADS, Workload, make_inputs
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not cuda_ok(), reason="needs a CUDA device")]
@@ -100,3 +100,84 @@ def test_stalled_grid_barrier_reports_timeout_and_context_survives():
     assert_bf16_close(host64(out["F_pre"]), ref["F_pre"], "F_pre")
     assert_bf16_close(host64(out["X_next"]), ref["X_next"], "X_next")
     assert mhc.mhc_device_status() == mhc.MHC_OK
+
+
+def _forward_ws(inp, wl, out, ws, stalled=False, stream=None):
+    args = (inp["Xd"], inp["phid"], inp["Fd"], wl.alpha_pre, wl.alpha_post, wl.alpha_res,
+            inp["biasd"], wl.iters, wl.B, wl.n, wl.C, out["Y"], out["r"], out["H_pre"],
+            out["H_post"], out["H_res"], out["F_pre"], out["X_next"], ws)
+    if stalled:
+        mhc.mhc_testing_forward_decode_stalled(*args, 50_000_000, stream=stream)
+    else:
+        mhc.mhc_testing_forward_decode(*args, stream=stream)
+
+
+def _device_inputs(wl, seed):
+    inp = make_inputs(wl, seed=seed)
+    inp.update(Xd=dev_bf16(inp["X"]), phid=dev_bf16(inp["phi_t"]), Fd=dev_bf16(inp["F_out"]),
+               biasd=dev_f32(inp["bias"]))
+    return inp
+
+
+@pytest.mark.parametrize("wl_name", ["decode8", "decode128"])
+def test_grid_barrier_words_clear_themselves(wl_name):
+    """The small-batch kernel's grid barrier needs no zeroed workspace: its
+    words carry the launch's epoch, start from whatever the workspace holds
+    and are 0 again when the kernel ends, after a completed barrier and after
+    one whose wait ran out."""
+    wl = WORKLOADS[wl_name]
+    inp = _device_inputs(wl, seed=12)
+    ref_out = mhc.alloc_outputs(wl.B, wl.n, wl.C)
+    _forward_ws(inp, wl, ref_out, ref_out["ws"])
+    torch.cuda.synchronize()
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+    out = {k: torch.empty_like(v) for k, v in ref_out.items()}
+    ws = out["ws"]
+    for fill in (0xA5, 0x00, 0xFF):
+        ws.fill_(fill)
+        _forward_ws(inp, wl, out, ws)
+        torch.cuda.synchronize()
+        assert mhc.mhc_device_status() == mhc.MHC_OK
+        assert not bool(ws[:16].any()), "barrier words left set"
+        for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre", "X_next"):
+            assert torch.equal(out[k], ref_out[k]), k
+    _forward_ws(inp, wl, out, ws, stalled=True)
+    torch.cuda.synchronize()
+    assert mhc.mhc_device_status() == mhc.MHC_ERR_TIMEOUT
+    assert not bool(ws[:16].any()), "barrier words left set after a timeout"
+    _forward_ws(inp, wl, out, ws)
+    torch.cuda.synchronize()
+    assert mhc.mhc_device_status() == mhc.MHC_OK
+    for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre", "X_next"):
+        assert torch.equal(out[k], ref_out[k]), k
+
+
+@pytest.mark.parametrize("B", [32, 512])
+def test_grid_barrier_in_a_replayed_graph(B):
+    """A CUDA graph fixes the launch's epoch, so every replay meets words that
+    the previous replay cleared; the replays give the eager call's bits.  At
+    B = 512 the X_next kernel runs between two launches of the small-batch
+    kernel."""
+    wl = Workload(f"decode{B}", B=B, n=4, C=7168)
+    inp = _device_inputs(wl, seed=13)
+    ref_out = mhc.alloc_outputs(wl.B, wl.n, wl.C)
+    _forward_ws(inp, wl, ref_out, ref_out["ws"])
+    torch.cuda.synchronize()
+    out = {k: torch.zeros_like(v) for k, v in ref_out.items()}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(g, stream=side):
+            for _ in range(3):
+                _forward_ws(inp, wl, out, out["ws"], stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(4):
+        for k in ("Y", "H_res", "F_pre", "X_next"):
+            out[k].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert mhc.mhc_device_status() == mhc.MHC_OK
+        assert not bool(out["ws"][:16].any())
+        for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre", "X_next"):
+            assert torch.equal(out[k], ref_out[k]), k
