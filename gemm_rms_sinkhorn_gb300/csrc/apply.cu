@@ -12,15 +12,18 @@
 // the token's coefficients are staged once per block in shared memory.
 // Streaming cache hints (.cs) keep the single-use data from displacing L2.
 //
-// Wide n (5..8) runs a few waves' worth of blocks instead, each walking the
-// tokens b, b + gridDim.y, ...: while it mixes one token, the next token's
-// coefficients are already on their way (into shared memory by cp.async for
-// post/res, into registers for pre), and for post/res its X and F_out into
-// L2 (prefetch), so a token does not wait for a coefficient round trip before
-// its DRAM round trip.  Measured at n = 8, C = 4096, B = 2048..8192 against
-// one token per block: post/res 11-14 % faster with the prefetch and two
-// waves (without the prefetch it gains 5-10 %), pre 2-6 % faster without a
-// prefetch and four waves (with one it lost at one wave).
+// Wide n (5..8) runs a set number of waves' worth of blocks instead, each
+// walking the tokens b, b + gridDim.y, ...: while it mixes one token, the
+// next token's coefficients are already on their way (into shared memory by
+// cp.async for post/res, into registers for pre), and for post/res its X and
+// F_out into L2 (prefetch), so a token does not wait for a coefficient round
+// trip before its DRAM round trip.  Measured at n = 8, C = 4096: against one
+// token per block, post/res 11-14 % faster with the prefetch (B = 2048..8192).
+// Its walks are best at about 6 tokens: at B = 8192, 178 µs at 27 tokens a
+// walk, 172 at 4-7, 176 at 2, 193 at 1 (nothing left to hide the next token
+// behind); 2-5 % faster than a fixed two waves at B = 3072..16384, the same
+// below.  Pre is fastest at one token per block (95 µs at B = 8192 with walks
+// of 7 tokens, 90-91 µs with 1-2), so it takes 32 waves.
 //
 // In place: X_next may equal X.  Every thread loads all its inputs before it
 // stores, and the addresses it stores are exactly the ones it loaded, which
@@ -240,11 +243,13 @@ dim3 apply_grid(int64_t B, int64_t C8, int threads)
     return dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy), 1);
 }
 
-// The wide kernels' grid: as many token rows as `waves` waves of resident
-// blocks hold (blocks per SM from the occupancy calculator, kept per kernel
-// and block size; SMs of the current device).
+// The wide kernels' grid: a whole number of waves of resident blocks (blocks
+// per SM from the occupancy calculator, kept per kernel and block size; SMs
+// of the current device), the number that gives each block's walk about
+// `walk` tokens, kept within [lo, hi] waves.  A partial last wave leaves SMs
+// idle at the end (measured at n = 8, B = 2048: 2.24 waves 10 % slower than 2).
 template <typename K>
-cudaError_t wide_grid(K kernel, int64_t B, int64_t C8, int threads, int waves,
+cudaError_t wide_grid(K kernel, int64_t B, int64_t C8, int threads, int walk, int lo, int hi,
                       std::atomic<int> *cache, dim3 &grid)
 {
     grid = apply_grid(B, C8, threads);
@@ -259,7 +264,11 @@ cudaError_t wide_grid(K kernel, int64_t B, int64_t C8, int threads, int waves,
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t rows = (static_cast<int64_t>(sms) * per_sm * waves + grid.x - 1) / grid.x;
+    const int64_t wave_rows = (static_cast<int64_t>(sms) * per_sm + grid.x - 1) / grid.x;
+    int64_t waves = (B + walk * wave_rows / 2) / (walk * wave_rows);  // rounded to nearest
+    if (waves < lo) waves = lo;
+    if (waves > hi) waves = hi;
+    const int64_t rows = waves * wave_rows;
     if (rows < grid.y) grid.y = static_cast<unsigned>(rows < 1 ? 1 : rows);
     return cudaSuccess;
 }
@@ -286,7 +295,7 @@ cudaError_t launch_post_res(const uint16_t *X, const FT *F_out, const float *H_r
 #define MHC_CASE(k)                                                                            \
     case k: {                                                                                  \
         dim3 g;                                                                                \
-        const cudaError_t e = wide_grid(post_res_apply_wide_kernel<k, FT>, B, C8, threads, 2,  \
+        const cudaError_t e = wide_grid(post_res_apply_wide_kernel<k, FT>, B, C8, threads, 6, 2, 16, \
                                         &per_sm[k - 5][threads_slot(threads)], g);             \
         if (e != cudaSuccess) return e;                                                        \
         return launch_pdl(post_res_apply_wide_kernel<k, FT>, g, dim3(threads), 0, stream, X,   \
@@ -315,7 +324,7 @@ cudaError_t launch_pre_apply(const uint16_t *X, const float *H_pre, int64_t B, i
 #define MHC_CASE(k)                                                                            \
     case k: {                                                                                  \
         dim3 g;                                                                                \
-        const cudaError_t e = wide_grid(pre_apply_wide_kernel<k>, B, C8, threads, 4,           \
+        const cudaError_t e = wide_grid(pre_apply_wide_kernel<k>, B, C8, threads, 1, 32, 32,       \
                                         &per_sm[k - 5][threads_slot(threads)], g);             \
         if (e != cudaSuccess) return e;                                                        \
         return launch_pdl(pre_apply_wide_kernel<k>, g, dim3(threads), 0, stream, X, H_pre, B,  \
