@@ -240,6 +240,24 @@ def test_wide_apply_token_walk_is_exact():
     assert np.array_equal(host_bits(out).reshape(B, n, C), want)
 
 
+@pytest.mark.parametrize("n", [5, 8])
+def test_pre_apply_long_walk_is_exact(n):
+    """The wide pre kernel runs 32 waves of blocks, one token per block up to
+    that many rows; 160001 tokens of 64 channels (8-channel items, 128-thread
+    blocks, at most 16 resident per SM) make every block row walk about two
+    tokens, so the register-held next H_pre is used.  One-hot H_pre per token:
+    a coefficient from the wrong token moves a whole stream."""
+    B, C = 160001, 64
+    X = synth.normal_bf16((B, n * C), 30, 0)
+    sel = np.random.default_rng(31).integers(0, n, size=B)
+    Hp = np.zeros((B, n), dtype=np.float32)
+    Hp[np.arange(B), sel] = 1.0
+    F = torch.empty(B, C, dtype=torch.bfloat16, device="cuda")
+    mhc.mhc_pre_apply(dev_bf16(X), dev_f32(Hp), B, n, C, F)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bits(F), X.reshape(B, n, C)[np.arange(B), sel, :])
+
+
 def test_post_res_apply_permutation_is_exact():
     B, n, C = 5, 3, 64
     X = synth.normal_bf16((B, n * C), 24, 0)
