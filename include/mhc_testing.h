@@ -83,8 +83,10 @@ int mhc_testing_forward_decode(const mhc_bf16 *X, const mhc_bf16 *phi_t, const m
  * than there are CTAs, so every CTA's wait runs out after `wait_limit_ns`
  * nanoseconds of GPU time (clamped to [1 ms, 4 s]).  Each CTA then records
  * MHC_ERR_TIMEOUT in the device status word (read with mhc_device_status)
- * and returns without writing Y, r, H or F_pre; the X_next kernel still runs
- * on whatever H_res and H_post hold.  The CUDA context stays usable.
+ * and returns without writing Y, r, H or F_pre, nor X_next up to 256 tokens;
+ * above that the X_next kernel still runs on whatever H_res and H_post hold.
+ * The barrier's words are left clear, so the next call on the same workspace
+ * works normally.  The CUDA context stays usable.
  */
 int mhc_testing_forward_decode_stalled(const mhc_bf16 *X, const mhc_bf16 *phi_t,
                                        const mhc_bf16 *F_out, float alpha_pre, float alpha_post,
