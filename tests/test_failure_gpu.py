@@ -87,8 +87,9 @@ def test_stalled_grid_barrier_reports_timeout_and_context_survives():
     assert mhc.mhc_device_status() == mhc.MHC_OK
     out = _forward(inp, wl, stalled=True)
     assert mhc.mhc_device_status() == mhc.MHC_ERR_TIMEOUT
-    # no CTA passed the barrier, so nothing of steps 1-4a was written
-    for k in ("Y", "r", "H_pre", "H_post", "H_res"):
+    # no CTA passed the barrier, so nothing of steps 1-4a was written, nor
+    # X_next, which the same kernel forms at this batch size
+    for k in ("Y", "r", "H_pre", "H_post", "H_res", "F_pre", "X_next"):
         assert not bool(out[k].any()), k
     assert mhc.mhc_device_status() == mhc.MHC_OK
     out = _forward(inp, wl)
