@@ -358,6 +358,13 @@ def forward_latency(mhc, step, stream, barrier, steps, warmup) -> dict:
 def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out) -> dict:
     """Mean CUDA-event time (ms) of each kernel over `steps` passes of the three
     entry points of the chain, events recorded between launches on the launching stream."""
+    runs = per_kernel_runs(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out)
+    return {k: statistics.mean(v) for k, v in runs.items()}
+
+
+def per_kernel_runs(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out) -> dict:
+    """CUDA-event time (ms) of each kernel in each of `steps` passes of the three
+    entry points of the chain (a list per kernel)."""
     import torch
 
     B, n, C = wl.B, wl.n, wl.C
@@ -377,7 +384,7 @@ def per_kernel_times(mhc, stream, barrier, steps, wl, X, phi_t, F_out, bias, out
                                stream)
         e[3].record(stream)
     barrier()
-    return {k: statistics.mean(evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps))
+    return {k: [evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]
             for i, k in enumerate(KERNELS)}
 
 
@@ -692,8 +699,8 @@ def main() -> int:
     value = tokens_per_second(B, world, args.steps, ms_total)
 
     # ---- per-kernel CUDA-event times over the same steps (same stream)
-    per_kernel_ms = per_kernel_times(mhc, stream, barrier, args.steps, wl, X, phi_t, F_out, bias,
-                                     out)
+    runs = per_kernel_runs(mhc, stream, barrier, args.steps, wl, X, phi_t, F_out, bias, out)
+    per_kernel_ms = {k: statistics.mean(v) for k, v in runs.items()}
     sampler.stop()
     status = mhc.mhc_device_status()
     if status != mhc.MHC_OK:
@@ -704,7 +711,10 @@ def main() -> int:
     dom = max(KERNELS, key=lambda k: per_kernel_ms[k])
     achieved = algo[dom] / (per_kernel_ms[dom] / 1e3) / 1e9
     total_bytes = sum(algorithmic_bytes(B, n, C).values())  # the steps' compulsory bytes
-    kernels_json = {k: {"ms": per_kernel_ms[k], "algorithmic_bytes": algo[k],
+    # "ms" is the mean over the steps (the roofline's average launch); the
+    # median and the fastest step are there beside it
+    kernels_json = {k: {"ms": per_kernel_ms[k], "median_ms": statistics.median(runs[k]),
+                        "min_ms": min(runs[k]), "algorithmic_bytes": algo[k],
                         "GBps": algo[k] / (per_kernel_ms[k] / 1e3) / 1e9,
                         "frac": algo[k] / (per_kernel_ms[k] / 1e3) / 1e9 / peak}
                     for k in KERNELS}
