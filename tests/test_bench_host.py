@@ -127,3 +127,40 @@ def test_oracle_on_all_cores_covers_every_token_once():
     for k in ("Y", "H_res", "X_next"):
         parts = np.concatenate([got[key][k] for key in sorted(got)])
         assert np.array_equal(parts, whole[k])
+
+
+def test_stored_traffic_follows_the_source_digest(tmp_path, monkeypatch):
+    """roofline.traffic comes from the committed counters only while the kernel's
+    source and the shared headers are those the counters were taken from: a
+    change to either makes it null."""
+    csrc = tmp_path / "gemm_rms_sinkhorn_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    (csrc / "apply.cu").write_text("kernel v1\n")
+    (csrc / "gemm_rms.cu").write_text("gemm v1\n")
+    (csrc / "ptx.cuh").write_text("header v1\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = bench.source_digest("post_res_apply")
+    assert digest == bench.source_digest("pre_apply")  # same .cu file
+    assert digest != bench.source_digest("gemm_rms")
+    entry = {"bytes_per_launch": 123, "source_sha256_16": digest, "workload": "w"}
+    (tmp_path / "profiles" / "dram_traffic.json").write_text(json.dumps({"post_res_apply": entry}))
+    assert bench.stored_traffic("post_res_apply") == 123
+    assert bench.stored_traffic("gemm_rms") is None  # no entry
+    (csrc / "ptx.cuh").write_text("header v2\n")  # a shared header changed
+    assert bench.stored_traffic("post_res_apply") is None
+    (csrc / "ptx.cuh").write_text("header v1\n")
+    (csrc / "apply.cu").write_text("kernel v2\n")  # the kernel's own file changed
+    assert bench.stored_traffic("post_res_apply") is None
+
+
+def test_committed_traffic_entries_are_well_formed():
+    """Every committed entry names a timed kernel, a positive byte count and a
+    16-hex-digit digest."""
+    with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+        d = json.load(f)
+    for k in bench.KERNELS:
+        ent = d[k]
+        assert int(ent["bytes_per_launch"]) > 0
+        assert len(ent["source_sha256_16"]) == 16
+        int(ent["source_sha256_16"], 16)
